@@ -1,0 +1,96 @@
+"""Seeded synthetic inputs for the decode MoE-layer tail.
+
+This module only draws random numbers and stores them in the layouts the
+library takes.  It holds none of the method's arithmetic (no GEMM, no top-k,
+no softmax, no normalisation), so both the CUDA path and the CPU oracle may be
+fed from it.
+
+Value recipe (shapes and distributions of the GLM-5.x decode, MTP-verify and
+prefill layer shapes; the second parameter of N(0, s) is a standard
+deviation):
+
+* hidden states x and residual ~ N(0, 1) * s, s in {1, 4};
+* gate weight W [E, H] ~ N(0, 0.02);
+* unfinalized expert rows [N, H] ~ N(0, 0.5), N = T*k rows unless padded;
+* expanded-index map [T, k]: a random permutation of the row buffer;
+* shared-expert output ~ N(0, 1);
+* gamma = 1 + 0.1 * N(0, 1) in FP32; eps = 1e-6;
+* row-parallel partials [R, T, H] ~ N(0, 0.25);
+* supplied router logits (prefill) ~ N(0, 0.02 * sqrt(H)) in FP32, the spread
+  of x . W at these scales;
+* stand-alone routing weights (used when the finalize step is exercised
+  without the routing step) ~ U(0, 2 * scale / k) in FP32.
+
+Activations are drawn in float64, narrowed to float32 and then to BF16 with
+round-to-nearest-even on the bit pattern.  Every array is reproducible from
+(seed, shape, s).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = ["to_bf16_bits", "draw_bf16", "tail_case", "CONFIGS"]
+
+
+def to_bf16_bits(a) -> np.ndarray:
+    """float64/float32 array -> BF16 bit patterns (uint16) via binary32, RNE."""
+    f = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    out = ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
+    return out
+
+
+def draw_bf16(rng: np.random.Generator, shape, std: float) -> np.ndarray:
+    return to_bf16_bits(rng.standard_normal(shape) * std)
+
+
+# Layer shapes of the five workloads: tiny, decode, MTP verify, prefill and
+# row-parallel partials.
+CONFIGS = {
+    "tiny": dict(T=[4], H=[2048], E=64, k=4, scale=1.0, seed=0, R=0),
+    "decode": dict(T=[1, 4, 64], H=[6144], E=256, k=8, scale=2.5, seed=1, R=0),
+    "verify": dict(T=[4, 12, 28], H=[6144, 2048], E=256, k=8, scale=2.5, seed=2, R=0),
+    "prefill": dict(T=[512, 2048, 8192], H=[6144], E=256, k=8, scale=2.5, seed=3, R=0),
+    "partials": dict(T=[1, 64, 2048], H=[6144], E=256, k=8, scale=2.5, seed=4, R=4),
+}
+
+
+def tail_case(T: int, H: int, E: int, k: int, *, seed: int, s: float = 1.0,
+              scale: float = 2.5, n_rows: int | None = None, shared: bool = True,
+              R: int = 0, router: bool = True, logits: bool = False,
+              weights: bool = True, eps: float = 1e-6) -> dict:
+    """Draw one layer's inputs.
+
+    Returns a dict of numpy arrays (BF16 as uint16 bit patterns):
+    ``x`` [T,H], ``w_gate`` [E,H] (if ``router``), ``rows`` [N,H], ``map``
+    [T,k] int32, ``topk_w`` [T,k] float32 (if ``weights``), ``shared`` [T,H]
+    or None, ``partials`` [R,T,H] or None, ``residual`` [T,H], ``gamma`` [H]
+    float32, ``logits`` [T,E] float32 (if ``logits``), and the scalars.
+    """
+    rng = np.random.default_rng([int(seed), int(T), int(H), int(E), int(k),
+                                 int(round(s * 16)), int(R)])
+    N = T * k if n_rows is None else int(n_rows)
+    if N < T * k:
+        raise ValueError("the row buffer must hold at least T*k rows")
+    case = dict(T=T, H=H, E=E, k=k, scale=float(scale), eps=float(eps), s=float(s),
+                n_rows=N, R=R)
+    case["x"] = draw_bf16(rng, (T, H), 1.0 * s)
+    case["w_gate"] = draw_bf16(rng, (E, H), 0.02) if router else None
+    case["rows"] = draw_bf16(rng, (N, H), 0.5)
+    case["map"] = rng.permutation(N)[: T * k].reshape(T, k).astype(np.int32)
+    case["shared"] = draw_bf16(rng, (T, H), 1.0) if shared else None
+    case["partials"] = draw_bf16(rng, (R, T, H), 0.25) if R > 0 else None
+    case["residual"] = draw_bf16(rng, (T, H), 1.0 * s)
+    case["gamma"] = (1.0 + 0.1 * rng.standard_normal(H)).astype(np.float32)
+    if weights:
+        hi = 2.0 * scale / max(k, 1)
+        case["topk_w"] = rng.uniform(0.0, hi, size=(T, k)).astype(np.float32)
+    else:
+        case["topk_w"] = None
+    if logits:
+        case["logits"] = (rng.standard_normal((T, E)) * (0.02 * np.sqrt(H))).astype(np.float32)
+    else:
+        case["logits"] = None
+    return case
