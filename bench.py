@@ -1,0 +1,566 @@
+#!/usr/bin/env python3
+"""Benchmark of the decode MoE-layer tail on GB300 (one JSON line on stdout).
+
+Headline workload: the decode tail of one MoE layer at T=64 tokens, H=6144,
+E=256 routed experts, top-8, one shared expert -- router GEMM (BF16 x BF16 ->
+FP32 logits), top-k routing (softmax over the top-8 x 2.5), then the fused
+finalize + shared add + residual add + RMSNorm.  One step is one layer; the
+steps walk through 75 distinct layers' buffers (gate weights, activations,
+expert rows: about 1 GB, several times the L2), so every step reads cold HBM.
+Steps are replayed from a CUDA graph and timed with CUDA events on the
+launching stream.  The metric is microseconds per layer (lower is better).
+
+Extra keys: ``roofline`` (the dominant kernel's algorithmic GB/s against the
+measured HBM copy peak), ``e2e`` (the same step with pinned-host inputs copied
+in and outputs copied out inside the timed region), ``clocks``,
+``cpu_baseline`` (the FP64 oracle on the host cores, a bounded sample) and
+``sweep`` (decode / verify / prefill / partial-sum shapes, T = 1..8192).
+
+``--impl reference`` times the CPU oracle on the same workload instead.
+Multi-GPU (torchrun): every rank runs the same per-rank workload as an
+independent replica (token rows need no exchange); the step time is the
+maximum over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs/layer and HBM GB/s (% of GB300 peak) for fused MoE tail, T=1..8192"
+UNIT = "µs/layer"
+T_DEC, H_DEC, E_DEC, K_DEC, SCALE = 64, 6144, 256, 8, 2.5
+N_LAYERS = 75  # distinct layer buffer sets the steps rotate through
+WORKLOAD = ("decode tail T=64 H=6144 E=256 k=8 +1 shared expert: router GEMM -> top-k route -> "
+            "finalize+shared+residual+RMSNorm")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the T=1..8192 sweep")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--min-timed-s", type=float, default=1.0,
+                    help="repeat the K-step timed region until this much time is covered")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (each input read once, each output written once)
+# ---------------------------------------------------------------------------
+
+def bytes_tail(T, H, k, shared=True, R=0, E=0, route_out=False):
+    per_tok = k * H * 2 + (H * 2 if shared else 0) + H * 2 + 8 * k + 2 * H * 2 + R * H * 2
+    if E:
+        per_tok += 4 * E - 4 * k  # logits instead of the weights
+        if route_out:
+            per_tok += 8 * k
+    return T * per_tok + 4 * H
+
+
+def bytes_router(T, H, E):
+    return E * H * 2 + T * H * 2 + T * E * 4
+
+
+def bytes_route(T, E, k):
+    return T * E * 4 + T * k * 8
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, ncu traffic
+# ---------------------------------------------------------------------------
+
+def load_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_tag, units_per_launch):
+    """Per-launch DRAM bytes from the committed ncu summary of `kernel_tag`,
+    scaled to `units_per_launch`; None if absent or the source changed since."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    if not os.path.exists(path):
+        return None
+    info = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- ") and ": " in line:
+                kk, vv = line[2:].split(": ", 1)
+                info[kk.strip()] = vv.strip().strip("`")
+    try:
+        files = info["source_files"].split()
+        if source_digest(files) != info["source_sha256"]:
+            return None
+        per_unit = float(info["dram_bytes_per_launch"]) / float(info["units_per_launch"])
+        return per_unit * units_per_launch
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# timing helpers
+# ---------------------------------------------------------------------------
+
+def capture(torch, fn, stream):
+    """CUDA graph of fn() captured on `stream` (after one eager warm-up run)."""
+    with torch.cuda.stream(stream):
+        fn()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def time_replays(torch, graphs_and_counts, stream):
+    """Replay [(graph, n)] in order once; returns elapsed ms (CUDA events)."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for g, n in graphs_and_counts:
+            for _ in range(n):
+                g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def graph_time_per_unit(torch, fn_per_set, nsets, stream, min_ms=150.0, min_reps=10):
+    """Capture one graph that runs fn_per_set(i) for every buffer set i, then
+    replay it until min_ms is covered; returns (median µs per set, p20, p80)."""
+    g = capture(torch, lambda: [fn_per_set(i) for i in range(nsets)], stream)
+    for _ in range(2):
+        g.replay()
+    stream.synchronize()
+    per, total = [], 0.0
+    while len(per) < min_reps or total < min_ms:
+        ms = time_replays(torch, [(g, 1)], stream)
+        per.append(ms * 1000.0 / nsets)
+        total += ms
+        if len(per) > 2000:
+            break
+    per.sort()
+    q = lambda f: per[min(len(per) - 1, int(f * len(per)))]
+    return statistics.median(per), q(0.2), q(0.8)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (there is no CPU path)")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import moe_decode_layer_logits_gb300 as M
+    from moe_decode_layer_logits_gb300.inputs import device_layer
+    from moe_decode_layer_logits_gb300.sharding import max_over_ranks
+    M.lib()
+
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
+    peak, peak_kind = load_peak()
+
+    # -- headline buffers: 75 layers, each its own gate weight and activations
+    layers = [device_layer(T_DEC, H_DEC, E_DEC, K_DEC, seed=1000 * rank + i, scale=SCALE) for i in range(N_LAYERS)]
+    torch.cuda.synchronize()
+    s = stream.cuda_stream
+
+    def router(d):
+        M.moe_router_logits_fp32(d["x"], d["w_gate"], logits_out=d["logits"], stream=s)
+
+    def route(d):
+        M.moe_topk_route(d["logits"], K_DEC, SCALE, topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
+
+    def finalize(d):
+        M.moe_finalize_add_rmsnorm(d["rows"], d["map"], d["topk_w"], d["shared"], d["residual"], d["gamma"],
+                                   d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"], stream=s)
+
+    def step(i):
+        d = layers[i % N_LAYERS]
+        router(d)
+        route(d)
+        finalize(d)
+
+    # warm-up: W untimed steps (eager), then graphs
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    stream.synchronize()
+    K = args.steps
+    g_full = capture(torch, lambda: [step(i) for i in range(N_LAYERS)], stream)
+    rem = K % N_LAYERS
+    g_rem = capture(torch, lambda: [step(i) for i in range(rem)], stream) if rem else None
+    plan = [(g_full, K // N_LAYERS)] + ([(g_rem, 1)] if g_rem else [])
+    for _ in range(max(1, args.warmup // N_LAYERS)):
+        g_full.replay()
+    stream.synchronize()
+
+    # -- timed region: exactly K steps, repeated to cover --min-timed-s
+    times = []
+    with ClockSampler(local) as clk:
+        while len(times) < 3 or sum(times) < args.min_timed_s * 1000.0:
+            if world > 1:
+                dist.barrier()
+            torch.cuda.synchronize()
+            ms = time_replays(torch, plan, stream)
+            torch.cuda.synchronize()
+            if world > 1:
+                dist.barrier()
+            times.append(max_over_ranks(ms))
+            if len(times) >= 200:
+                break
+    clocks = clk.summary()
+    ms_region = statistics.median(times)
+    us_layer = ms_region * 1000.0 / K
+
+    # -- per-kernel device time (each kernel alone, same cold rotation)
+    kern = {}
+    kern["finalize"] = graph_time_per_unit(torch, lambda i: finalize(layers[i]), N_LAYERS, stream)
+    kern["router"] = graph_time_per_unit(torch, lambda i: router(layers[i]), N_LAYERS, stream)
+    kern["route"] = graph_time_per_unit(torch, lambda i: route(layers[i]), N_LAYERS, stream)
+    b = {"finalize": bytes_tail(T_DEC, H_DEC, K_DEC), "router": bytes_router(T_DEC, H_DEC, E_DEC),
+         "route": bytes_route(T_DEC, E_DEC, K_DEC)}
+    dom = max(kern, key=lambda n: kern[n][0])
+    dom_us = kern[dom][0]
+    achieved = b[dom] / (dom_us * 1e-6) / 1e9
+    tag = {"finalize": "tail_kernel_decode_T64", "router": "router_kernel_decode_T64",
+           "route": "topk_route_kernel_decode_T64"}[dom]
+    traffic = ncu_traffic(tag, T_DEC)
+
+    # -- fused variant: router + router-less fused tail
+    def fused_step(i):
+        d = layers[i]
+        router(d)
+        M.moe_tail_fused(d["logits"], K_DEC, SCALE, d["rows"], d["map"], d["shared"], d["residual"], d["gamma"],
+                         d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"],
+                         topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
+    fused_us = graph_time_per_unit(torch, fused_step, N_LAYERS, stream)
+
+    # -- end to end through the C ABI with pinned host buffers
+    e2e = run_e2e(torch, M, layers, stream, K, args.warmup)
+
+    del layers
+    torch.cuda.empty_cache()
+    sweep = None if args.no_sweep else run_sweep(torch, M, stream, l2, peak)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(budget_s=10.0)
+
+    line = {
+        "metric": METRIC, "value": round(us_layer, 4), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(us_layer / 1000.0, 7), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "io_dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": T_DEC, "H": H_DEC, "E": E_DEC, "k": K_DEC, "routed_scale": SCALE,
+                   "layers_rotated": N_LAYERS,
+                   "l2": f"cold: {N_LAYERS} layer buffer sets, {N_LAYERS * 13.5:.0f} MB > L2 {l2 / 2**20:.0f} MB",
+                   "timing": "CUDA-graph replay, CUDA events on the launching stream",
+                   "parallelism": f"replicas x{world}"},
+        "repeats": len(times), "gpu_launches": 3 * K,
+        "clocks": clocks,
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} (hbm_gbs)", "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "algorithmic_bytes_per_launch": b[dom], "launch_us": round(dom_us, 3),
+                     "traffic": None if traffic is None else round(traffic)},
+        "kernels_us": {n: {"median": round(v[0], 3), "p20": round(v[1], 3), "p80": round(v[2], 3),
+                           "GBps": round(b[n] / (v[0] * 1e-6) / 1e9, 1)} for n, v in kern.items()},
+        "fused_variant_us_per_layer": {"median": round(fused_us[0], 3), "p20": round(fused_us[1], 3),
+                                       "p80": round(fused_us[2], 3),
+                                       "what": "router GEMM -> router-less fused tail (2 launches)"},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "sweep": sweep,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(torch, M, layers, stream, K, warmup):
+    """Same step, host buffers: H2D of the step's activations from pinned host
+    memory, the three C-ABI calls, D2H of both outputs; timed with events."""
+    d0 = layers[0]
+    names_in = ["x", "rows", "map", "shared", "residual"]
+    host_in = {n: torch.empty_like(d0[n], device="cpu").pin_memory() for n in names_in}
+    for n in names_in:
+        host_in[n].copy_(d0[n].cpu())
+    host_out = {n: torch.empty_like(d0[n], device="cpu").pin_memory() for n in ["residual_out", "normed_out"]}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    s = stream.cuda_stream
+    n_steps = max(1, min(K, 750))
+
+    def one(i):
+        d = layers[i % len(layers)]
+        with torch.cuda.stream(stream):
+            for n in names_in:
+                d[n].copy_(host_in[n], non_blocking=True)
+            M.moe_router_logits_fp32(d["x"], d["w_gate"], logits_out=d["logits"], stream=s)
+            M.moe_topk_route(d["logits"], K_DEC, SCALE, topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
+            M.moe_finalize_add_rmsnorm(d["rows"], d["map"], d["topk_w"], d["shared"], d["residual"], d["gamma"],
+                                       d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"],
+                                       stream=s)
+            host_out["residual_out"].copy_(d["residual_out"], non_blocking=True)
+            host_out["normed_out"].copy_(d["normed_out"], non_blocking=True)
+
+    for i in range(max(warmup, 3)):
+        one(i)
+    stream.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n_steps):
+        one(i)
+    e1.record(stream)
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / n_steps
+    return {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n_steps, "what": "pinned host -> device copies, 3 C-ABI calls, device -> pinned host copies"}
+
+
+def run_sweep(torch, M, stream, l2, peak):
+    """µs and GB/s of the tail over the decode / verify / prefill / partials shapes."""
+    from moe_decode_layer_logits_gb300.inputs import device_layer
+    s = stream.cuda_stream
+    out = []
+
+    def nsets_for(set_bytes):
+        return int(min(N_LAYERS, max(2, math.ceil(3 * l2 / set_bytes))))
+
+    def add(name, T, H, fn, nb, sets):
+        med, p20, p80 = graph_time_per_unit(torch, lambda i: fn(sets[i]), len(sets), stream, min_ms=100.0)
+        gbs = nb / (med * 1e-6) / 1e9
+        out.append({"case": name, "T": T, "H": H, "us": round(med, 3), "p20": round(p20, 3), "p80": round(p80, 3),
+                    "GBps": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "bytes": nb})
+
+    # decode + verify layers: full path (router -> route -> finalize) and fused
+    for T, H in [(1, 6144), (4, 6144), (64, 6144), (12, 6144), (28, 6144), (12, 2048), (28, 2048)]:
+        nb = bytes_router(T, H, E_DEC) + bytes_route(T, E_DEC, K_DEC) + bytes_tail(T, H, K_DEC)
+        sets = [device_layer(T, H, E_DEC, K_DEC, seed=7000 + i, scale=SCALE) for i in range(nsets_for(nb))]
+
+        def full(d):
+            M.moe_router_logits_fp32(d["x"], d["w_gate"], logits_out=d["logits"], stream=s)
+            M.moe_topk_route(d["logits"], K_DEC, SCALE, topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
+            M.moe_finalize_add_rmsnorm(d["rows"], d["map"], d["topk_w"], d["shared"], d["residual"], d["gamma"],
+                                       d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"],
+                                       stream=s)
+
+        def fin(d):
+            M.moe_finalize_add_rmsnorm(d["rows"], d["map"], d["topk_w"], d["shared"], d["residual"], d["gamma"],
+                                       d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"],
+                                       stream=s)
+        add("decode layer: router+route+finalize", T, H, full, nb, sets)
+        add("finalize+shared+residual+RMSNorm", T, H, fin, bytes_tail(T, H, K_DEC), sets)
+        del sets
+    # prefill: router-less fused tail on supplied logits, and finalize alone
+    for T in [512, 2048, 8192]:
+        H = 6144
+        nb = bytes_tail(T, H, K_DEC, E=E_DEC)
+        sets = [device_layer(T, H, E_DEC, K_DEC, seed=8000 + i, scale=SCALE, router=False, logits=True)
+                for i in range(nsets_for(nb))]
+        for d in sets:
+            M.moe_topk_route(d["logits"], K_DEC, SCALE, topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
+
+        def fused(d):
+            M.moe_tail_fused(d["logits"], K_DEC, SCALE, d["rows"], d["map"], d["shared"], d["residual"],
+                             d["gamma"], d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"],
+                             want_route=False, stream=s)
+
+        def fin(d):
+            M.moe_finalize_add_rmsnorm(d["rows"], d["map"], d["topk_w"], d["shared"], d["residual"], d["gamma"],
+                                       d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"],
+                                       stream=s)
+        add("prefill fused tail (logits supplied)", T, H, fused, nb, sets)
+        add("finalize+shared+residual+RMSNorm", T, H, fin, bytes_tail(T, H, K_DEC), sets)
+        del sets
+        torch.cuda.empty_cache()
+    # row-parallel partials: R=4 local partial buffers replace gather + shared
+    for T in [1, 64, 2048]:
+        H = 6144
+        nb = bytes_tail(T, H, 0, shared=False, R=4)
+        sets = [device_layer(T, H, E_DEC, 0, seed=9000 + i, shared=False, R=4, router=False)
+                for i in range(nsets_for(nb))]
+
+        def part(d):
+            M.moe_finalize_add_rmsnorm(None, None, None, None, d["residual"], d["gamma"], d["eps"],
+                                       partials=d["partials"], residual_out=d["residual_out"],
+                                       normed_out=d["normed_out"], stream=s)
+        add("R=4 partials+residual+RMSNorm", T, H, part, nb, sets)
+        del sets
+        torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs
+# ---------------------------------------------------------------------------
+
+_CPU_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
+
+
+def cpu_baseline(budget_s=10.0, n_tok=T_DEC, n_layers=None, warm=1):
+    """Time the FP64 oracle on decode layers in a single-threaded child process:
+    `warm` untimed layers, then `n_layers` timed layers, or as many as fit in
+    `budget_s` (at least one).  Each layer is router -> route -> tail on a
+    sample of `n_tok` of the 64 tokens; the time is scaled to 64 tokens."""
+    env = dict(os.environ, **_CPU_ENV)
+    code = (
+        "import sys,time,json; sys.path.insert(0, %r)\n"
+        "import oracle as O\n"
+        "from moe_decode_layer_logits_gb300.inputs import tail_case\n"
+        "c = tail_case(%d, %d, %d, %d, seed=1, weights=False)\n"
+        "def layer():\n"
+        "    L, A = O.router_logits(c['x'], c['w_gate'])\n"
+        "    ids, w, _ = O.topk_route(L.astype('float32'), %d, %r)\n"
+        "    O.finalize_add_rmsnorm(c['rows'], c['map'], w, c['shared'], None, c['residual'], c['gamma'], 1e-6)\n"
+        "for _ in range(%d): layer()\n"
+        "n_fixed, budget = %r, %r\n"
+        "n, t0 = 0, time.perf_counter()\n"
+        "while (n < n_fixed) if n_fixed else (n < 1 or time.perf_counter() - t0 < budget):\n"
+        "    layer(); n += 1\n"
+        "print(json.dumps({'s': time.perf_counter() - t0, 'n': n}))\n"
+    ) % (ROOT, n_tok, H_DEC, E_DEC, K_DEC, K_DEC, SCALE, warm, n_layers, budget_s)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True)
+    if r.returncode != 0:
+        return {"error": (r.stderr.strip().splitlines() or ["oracle failed"])[-1]}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    us = d["s"] * 1e6 / d["n"] * (T_DEC / n_tok)
+    return {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{d['n']} decode layers of {n_tok} of 64 tokens (H=6144, E=256, k=8), FP64 numpy, "
+                      f"{d['s']:.1f} s, single thread" + ("" if n_tok == T_DEC else f", time scaled x{T_DEC / n_tok:g}")}
+
+
+def run_reference(args):
+    """The oracle as it stands, on this workload: W untimed + exactly K timed
+    layers, each on a token sample sized so the run stays within minutes."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    probe = cpu_baseline(budget_s=0.0, n_layers=1)
+    full_us = probe.get("value") or 1e5
+    budget_per_step_us = 150e6 / max(1, args.steps + args.warmup)
+    n_tok = max(1, min(T_DEC, int(T_DEC * budget_per_step_us / full_us)))
+    while T_DEC % n_tok:
+        n_tok -= 1
+    res = cpu_baseline(n_tok=n_tok, n_layers=max(1, args.steps), warm=args.warmup)
+    v = res.get("value")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None if v is None else v / 1000.0,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "T": T_DEC, "H": H_DEC, "E": E_DEC, "k": K_DEC,
+                       "routed_scale": SCALE},
+            "cpu_baseline": res,
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,90 @@
+// Device helpers shared by the tail kernels: BF16 packing, streaming 16-byte
+// loads and the warp / block / cluster sum reductions with a fixed order.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cooperative_groups.h>
+#include <stdint.h>
+
+namespace moe {
+
+namespace cg = cooperative_groups;
+
+// Two BF16 values in one 32-bit word, low half first.
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// Round two floats to BF16 (nearest even) and pack them, `a` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 16-byte load through the read-only path that does not allocate in L1: the
+// data is read once per launch (expert rows, activations).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// 16-byte load of data that several CTAs re-read (gamma, the router input x).
+__device__ __forceinline__ uint4 ld_keep16(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ void st16(void* p, uint4 v) {
+  *reinterpret_cast<uint4*>(p) = v;
+}
+
+// Unpack 8 BF16 values of a 16-byte vector into floats.
+__device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
+  f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
+  f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+  f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
+  f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+  return v;
+}
+
+// Sum of one float per thread over the block.  Warp partials go to
+// scratch[warp]; thread 0 adds them in warp order, so every launch adds in
+// the same order.  Every thread gets the total.  `scratch` holds >= 33 floats.
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  v = warp_sum(v);
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < nwarps; ++w) s += scratch[w];
+    scratch[32] = s;
+  }
+  __syncthreads();
+  return scratch[32];
+}
+
+// Sum of one float per CTA over the thread-block cluster through distributed
+// shared memory.  `slot` is a shared float of this CTA that every CTA of the
+// cluster reads; all CTAs add the ranks in ascending order and so agree
+// bit for bit.  Must be called by every thread of every CTA in the cluster.
+__device__ __forceinline__ float cluster_sum(float cta_value, float* slot) {
+  cg::cluster_group cluster = cg::this_cluster();
+  if (threadIdx.x == 0) *slot = cta_value;
+  cluster.sync();
+  const unsigned n = cluster.num_blocks();
+  float s = 0.f;
+  for (unsigned r = 0; r < n; ++r) s += *cluster.map_shared_rank(slot, r);
+  cluster.sync();  // no CTA leaves while a peer may still read its slot
+  return s;
+}
+
+}  // namespace moe

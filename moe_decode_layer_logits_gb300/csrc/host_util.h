@@ -1,0 +1,28 @@
+// Host-side helpers of the C ABI: argument checks, the per-device SM-count
+// cache and the mapping of CUDA launch errors to status codes.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <math.h>
+
+#include "../../include/moe_tail.h"
+
+namespace moe {
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Number of SMs of the current device, queried once per device.
+int sm_count();
+
+// Status of the launch just made on this thread.
+inline int launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Largest number of tokens put on grid.y by one launch; the entry points loop
+// over larger T in chunks of this size.
+constexpr int64_t kMaxGridY = 65535;
+
+}  // namespace moe

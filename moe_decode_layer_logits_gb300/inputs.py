@@ -94,3 +94,37 @@ def tail_case(T: int, H: int, E: int, k: int, *, seed: int, s: float = 1.0,
     else:
         case["logits"] = None
     return case
+
+
+def device_layer(T: int, H: int, E: int, k: int, *, seed: int, s: float = 1.0, scale: float = 2.5,
+                 shared: bool = True, R: int = 0, router: bool = True, logits: bool = False,
+                 device="cuda") -> dict:
+    """The same recipe drawn directly on the GPU with a seeded torch generator
+    (for benchmark buffers too large to draw on the host).  BF16 tensors come
+    from FP32 draws rounded to nearest even; output buffers are allocated too.
+    """
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+
+    def bf16(shape, std):
+        return (torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std).to(torch.bfloat16)
+
+    N = T * k
+    d = dict(T=T, H=H, E=E, k=k, R=R, scale=float(scale), eps=1e-6)
+    d["x"] = bf16((T, H), 1.0 * s) if router else None
+    d["w_gate"] = bf16((E, H), 0.02) if router else None
+    d["rows"] = bf16((max(N, 1), H), 0.5)
+    d["map"] = torch.randperm(max(N, 1), generator=g, device=device, dtype=torch.int64)[:N].reshape(T, k).to(torch.int32)
+    d["shared"] = bf16((T, H), 1.0) if shared else None
+    d["partials"] = bf16((R, T, H), 0.25) if R > 0 else None
+    d["residual"] = bf16((T, H), 1.0 * s)
+    d["gamma"] = 1.0 + 0.1 * torch.randn(H, generator=g, device=device, dtype=torch.float32)
+    d["logits"] = (torch.randn((T, E), generator=g, device=device, dtype=torch.float32) * (0.02 * H ** 0.5)
+                   if logits else torch.empty((T, E), device=device, dtype=torch.float32))
+    d["topk_ids"] = torch.empty((T, max(k, 1)), device=device, dtype=torch.int32)
+    d["topk_w"] = torch.empty((T, max(k, 1)), device=device, dtype=torch.float32)
+    d["residual_out"] = torch.empty((T, H), device=device, dtype=torch.bfloat16)
+    d["normed_out"] = torch.empty((T, H), device=device, dtype=torch.bfloat16)
+    return d

@@ -1,0 +1,442 @@
+"""GPU parity: every entry point of the C ABI against the FP64 oracle.
+
+Inputs are the seeded synthetic layer shapes (tiny, decode T in {1,4,64},
+MTP verify T in {4,12,28} at H 6144 and 2048, prefill T in {512,2048,8192},
+R=4 row-parallel partials) plus ragged and edge cases.  Tolerances are
+derived in tests/_tol.py: router logits within 1e-5 * sum|x w|; top-k ids
+bit-exact on identical logits; BF16 outputs within one BF16 ulp of the
+oracle's once-rounded value (widened only by the FP32 forward-error bound).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from _tol import check_bf16, route_weight_tol, tail_deltas
+from moe_decode_layer_logits_gb300.inputs import draw_bf16, tail_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def M():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import os
+    from moe_decode_layer_logits_gb300 import build
+    if not os.path.exists(build.LIB):
+        build.build_library()
+    import moe_decode_layer_logits_gb300 as m
+    m.lib()
+    return m
+
+
+def dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def devf(a, dtype=torch.float32):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dtype).cuda()
+
+
+def bits(t):
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# router logits
+# ---------------------------------------------------------------------------
+
+ROUTER = [  # (T, H, E)
+    (4, 2048, 64), (1, 6144, 256), (4, 6144, 256), (64, 6144, 256), (12, 6144, 256), (28, 2048, 256),
+    (37, 2056, 72), (300, 6144, 256), (5, 512, 20), (3, 64, 1), (9, 1024, 1024), (16, 8, 16), (130, 6144, 168),
+]
+
+
+@pytest.mark.parametrize("T,H,E", ROUTER)
+def test_router_logits(M, T, H, E):
+    rng = np.random.default_rng([100, T, H, E])
+    x = draw_bf16(rng, (T, H), 1.0)
+    w = draw_bf16(rng, (E, H), 0.02)
+    L, A = O.router_logits(x, w)
+    g = M.moe_router_logits_fp32(dev(x), dev(w)).cpu().numpy().astype(np.float64)
+    err = np.abs(g - L)
+    assert np.all(err <= 1e-5 * A + 1e-30), float(np.max(err / np.maximum(A, 1e-30)))
+
+
+def test_router_prefill_size_sampled(M):
+    T, H, E = 8192, 6144, 256
+    rng = np.random.default_rng(101)
+    x = draw_bf16(rng, (T, H), 4.0)
+    w = draw_bf16(rng, (E, H), 0.02)
+    g = M.moe_router_logits_fp32(dev(x), dev(w)).cpu().numpy().astype(np.float64)
+    rows = np.sort(rng.choice(T, 256, replace=False))
+    rows[-1] = T - 1
+    L, A = O.router_logits(x[rows], w)
+    assert np.all(np.abs(g[rows] - L) <= 1e-5 * A)
+
+
+def test_router_small_integers_exact(M):
+    # every product and partial sum is an integer below 2^24: exact in FP32
+    rng = np.random.default_rng(102)
+    from moe_decode_layer_logits_gb300.inputs import to_bf16_bits
+    for T, H, E in [(64, 2048, 256), (3, 2048, 64), (33, 1000, 40)]:
+        xi = rng.integers(-16, 17, size=(T, H))
+        wi = rng.integers(-16, 17, size=(E, H))
+        g = M.moe_router_logits_fp32(dev(to_bf16_bits(xi)), dev(to_bf16_bits(wi))).cpu().numpy()
+        assert np.array_equal(g.astype(np.int64), xi @ wi.T)
+
+
+# ---------------------------------------------------------------------------
+# top-k routing on identical FP32 logits: ids bit-exact
+# ---------------------------------------------------------------------------
+
+ROUTE = [  # (T, E, k, scale)
+    (4, 64, 4, 1.0), (1, 256, 8, 2.5), (64, 256, 8, 2.5), (8192, 256, 8, 2.5), (37, 72, 3, 1.0),
+    (5, 1024, 32, 0.5), (7, 33, 32, 2.5), (3, 1, 1, 2.5), (11, 168, 8, 2.5), (9, 40, 32, 1.0),
+]
+
+
+def _check_route(M, lg, k, scale):
+    ids_g, w_g = M.moe_topk_route(devf(lg), k, scale)
+    ids_g = ids_g.cpu().numpy()
+    w_g = w_g.cpu().numpy().astype(np.float64)
+    ids, w32, w64 = O.topk_route(lg, k, scale)
+    assert np.array_equal(ids_g, ids)
+    tol = route_weight_tol(lg, ids, w64)
+    assert np.all(np.abs(w_g - w64) <= tol), float(np.max(np.abs(w_g - w64) / tol))
+
+
+@pytest.mark.parametrize("T,E,k,scale", ROUTE)
+def test_topk_route(M, T, E, k, scale):
+    rng = np.random.default_rng([200, T, E, k])
+    lg = (rng.standard_normal((T, E)) * 1.57).astype(np.float32)
+    _check_route(M, lg, k, scale)
+
+
+@pytest.mark.parametrize("E,k", [(64, 4), (256, 8), (9, 5)])
+def test_topk_route_ties(M, E, k):
+    # integer logits in [-2, 2]: many exact ties, resolved to the lower index
+    rng = np.random.default_rng([201, E, k])
+    lg = rng.integers(-2, 3, size=(257, E)).astype(np.float32)
+    lg[0] = 0.0
+    lg[1, :] = -0.0
+    lg[1, ::3] = 0.0
+    _check_route(M, lg, k, 2.5)
+
+
+# ---------------------------------------------------------------------------
+# finalize + shared add + partials + residual add + RMSNorm
+# ---------------------------------------------------------------------------
+
+def _oracle_tail(c, tok=None, w=None):
+    sl = slice(None) if tok is None else tok
+    mp = c["map"][sl] if c["k"] > 0 else np.zeros((c["T"] if tok is None else len(tok), 0), np.int32)
+    ww = (c["topk_w"] if w is None else w)[sl] if c["k"] > 0 else np.zeros((mp.shape[0], 0), np.float32)
+    sh = None if c["shared"] is None else c["shared"][sl]
+    pa = None if c["partials"] is None else c["partials"][:, sl]
+    return O.finalize_add_rmsnorm(c["rows"], mp, ww, sh, pa, c["residual"][sl], c["gamma"], c["eps"])
+
+
+def _run_finalize(M, c, residual_out=None, err_flag=None):
+    k = c["k"]
+    rows = dev(c["rows"]) if k > 0 else None
+    mp = torch.from_numpy(c["map"]).cuda() if k > 0 else None
+    w = devf(c["topk_w"]) if k > 0 else None
+    sh = dev(c["shared"]) if c["shared"] is not None else None
+    pa = dev(c["partials"]) if c["partials"] is not None else None
+    res = dev(c["residual"])
+    ro, no = M.moe_finalize_add_rmsnorm(rows, mp, w, sh, res, devf(c["gamma"]), c["eps"], partials=pa,
+                                        residual_out=res if residual_out == "alias" else None, err_flag=err_flag)
+    return bits(ro), bits(no)
+
+
+def _check_tail(c, ref, ro, no, extra_abs_r=None, tag="", max_widened_frac=0.01):
+    n_ops = c["k"] + (c["shared"] is not None) + c["R"] + 1
+    dr, dn = tail_deltas(ref, n_ops, c["gamma"], c["eps"], extra_abs_r)
+    a = check_bf16(tag + " residual_out", ro, ref["residual_out"], ref["r"], dr, max_widened_frac)
+    b = check_bf16(tag + " normed", no, ref["normed"], ref["normed64"], dn, max_widened_frac)
+    return a, b
+
+
+FIN = [  # name, T, H, E, k, extra kwargs
+    ("tiny-s1", 4, 2048, 64, 4, dict(scale=1.0, seed=0, s=1.0)),
+    ("tiny-s4", 4, 2048, 64, 4, dict(scale=1.0, seed=0, s=4.0)),
+    ("decode-1", 1, 6144, 256, 8, dict(seed=1)),
+    ("decode-4", 4, 6144, 256, 8, dict(seed=1, s=4.0)),
+    ("decode-64", 64, 6144, 256, 8, dict(seed=1)),
+    ("verify-4", 4, 6144, 256, 8, dict(seed=2)),
+    ("verify-12", 12, 6144, 256, 8, dict(seed=2, s=4.0)),
+    ("verify-28", 28, 6144, 256, 8, dict(seed=2)),
+    ("verify-12-h2048", 12, 2048, 256, 8, dict(seed=2)),
+    ("verify-28-h2048", 28, 2048, 256, 8, dict(seed=2, s=4.0)),
+    ("prefill-512", 512, 6144, 256, 8, dict(seed=3)),
+    ("partials-1", 1, 6144, 256, 0, dict(seed=4, R=4, shared=False)),
+    ("partials-64", 64, 6144, 256, 0, dict(seed=4, R=4, shared=False, s=4.0)),
+    ("mixed-gather-shared-partials", 16, 6144, 256, 8, dict(seed=5, R=3)),
+    ("shared-only", 9, 1024, 16, 0, dict(seed=6)),
+    ("no-shared", 9, 1024, 16, 8, dict(seed=7, shared=False)),
+    ("ragged", 37, 2056, 72, 5, dict(seed=8)),
+    ("padded-rows", 9, 768, 16, 8, dict(seed=9, n_rows=100)),
+    ("k16", 6, 512, 64, 16, dict(seed=10)),
+    ("k32", 5, 512, 64, 32, dict(seed=11, R=8)),
+    ("h8", 3, 8, 16, 2, dict(seed=12)),
+    ("h16384", 3, 16384, 16, 8, dict(seed=13)),
+    ("h65536", 2, 65536, 16, 4, dict(seed=14)),
+    ("t300", 300, 2048, 16, 8, dict(seed=15)),
+]
+
+
+@pytest.mark.parametrize("name,T,H,E,k,kw", FIN, ids=[f[0] for f in FIN])
+def test_finalize_add_rmsnorm(M, name, T, H, E, k, kw):
+    c = tail_case(T, H, E, k, router=False, **kw)
+    ref = _oracle_tail(c)
+    ro, no = _run_finalize(M, c)
+    _check_tail(c, ref, ro, no, tag=name)
+
+
+@pytest.mark.parametrize("T,kw", [(2048, dict(seed=3)), (8192, dict(seed=3)), (2048, dict(seed=4, R=4, shared=False, k0=True))])
+def test_finalize_full_size_sampled(M, T, kw):
+    kw = dict(kw)
+    k = 0 if kw.pop("k0", False) else 8
+    c = tail_case(T, 6144, 256, k, router=False, **kw)
+    ro, no = _run_finalize(M, c)
+    rng = np.random.default_rng(T)
+    tok = np.sort(rng.choice(T, 48, replace=False))
+    tok[0], tok[-1] = 0, T - 1
+    ref = _oracle_tail(c, tok)
+    _check_tail({**c, "shared": None if c["shared"] is None else c["shared"][tok]}, ref, ro[tok], no[tok],
+                tag=f"T={T}")
+
+
+def test_finalize_residual_out_may_alias_residual(M):
+    c = tail_case(12, 6144, 256, 8, router=False, seed=20)
+    ref = _oracle_tail(c)
+    ro, no = _run_finalize(M, c, residual_out="alias")
+    _check_tail(c, ref, ro, no, tag="alias")
+
+
+def test_finalize_bad_index_sets_flag_and_reads_zero(M):
+    c = tail_case(6, 1024, 16, 4, router=False, seed=21)
+    n = c["rows"].shape[0]
+    c["map"] = c["map"].copy()
+    c["map"][1, 2] = n          # one past the end
+    c["map"][4, 0] = -1         # negative
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ro, no = _run_finalize(M, c, err_flag=flag)
+    assert int(flag.item()) & 1
+    # the kernel never dereferences them: those rows count as zero
+    w = c["topk_w"].copy()
+    w[1, 2] = 0.0
+    w[4, 0] = 0.0
+    safe = c["map"].copy()
+    safe[1, 2] = 0
+    safe[4, 0] = 0
+    ref = _oracle_tail({**c, "map": safe}, w=w)
+    _check_tail(c, ref, ro, no, tag="bad-index")
+    # valid maps leave the flag alone
+    flag.zero_()
+    c2 = tail_case(6, 1024, 16, 4, router=False, seed=22)
+    _run_finalize(M, c2, err_flag=flag)
+    assert int(flag.item()) == 0
+
+
+def test_finalize_is_deterministic(M):
+    c = tail_case(64, 6144, 256, 8, router=False, seed=23)
+    a = _run_finalize(M, c)
+    b = _run_finalize(M, c)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_row_permutation_is_bitwise_invariant(M):
+    c = tail_case(28, 6144, 256, 8, router=False, seed=24)
+    a = _run_finalize(M, c)
+    perm = np.random.default_rng(3).permutation(c["rows"].shape[0])
+    rows2 = np.empty_like(c["rows"])
+    rows2[perm] = c["rows"]
+    b = _run_finalize(M, {**c, "rows": rows2, "map": perm[c["map"]].astype(np.int32)})
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ---------------------------------------------------------------------------
+# router-less fused tail
+# ---------------------------------------------------------------------------
+
+def _run_fused(M, c, want_route=True):
+    return M.moe_tail_fused(devf(c["logits"]), c["k"], c["scale"], dev(c["rows"]), torch.from_numpy(c["map"]).cuda(),
+                            dev(c["shared"]) if c["shared"] is not None else None, dev(c["residual"]),
+                            devf(c["gamma"]), c["eps"], want_route=want_route)
+
+
+def _check_fused(M, c, tok=None, tag=""):
+    ro, no, ids, w = _run_fused(M, c)
+    ro, no, ids, w = bits(ro), bits(no), ids.cpu().numpy(), w.cpu().numpy().astype(np.float64)
+    sl = slice(None) if tok is None else tok
+    lg = c["logits"][sl]
+    rids, rw32, rw64 = O.topk_route(lg, c["k"], c["scale"])
+    assert np.array_equal(ids[sl], rids)
+    wtol = route_weight_tol(lg, rids, rw64)
+    assert np.all(np.abs(w[sl] - rw64) <= wtol)
+    sh = None if c["shared"] is None else c["shared"][sl]
+    ref = O.finalize_add_rmsnorm(c["rows"], c["map"][sl], rw32, sh, None, c["residual"][sl], c["gamma"], c["eps"])
+    # the GPU weights may differ from the oracle's by wtol (+ half a binary32 ulp of rounding)
+    rows = O.bf16_bits_to_f64(c["rows"])
+    dw = wtol + np.abs(rw64) * 2.0 ** -24
+    extra = np.zeros_like(ref["r"])
+    for j in range(c["k"]):
+        extra += dw[:, j:j + 1] * np.abs(rows[c["map"][sl][:, j]])
+    return _check_tail({**c, "shared": sh}, ref, ro[sl], no[sl], extra_abs_r=extra, tag=tag)
+
+
+FUSED = [  # name, T, H, E, k, kw
+    ("tiny", 4, 2048, 64, 4, dict(scale=1.0, seed=0)),
+    ("decode-1", 1, 6144, 256, 8, dict(seed=1)),
+    ("decode-4", 4, 6144, 256, 8, dict(seed=1, s=4.0)),
+    ("decode-64", 64, 6144, 256, 8, dict(seed=1)),
+    ("verify-28", 28, 6144, 256, 8, dict(seed=2)),
+    ("verify-12-h2048", 12, 2048, 256, 8, dict(seed=2)),
+    ("prefill-512", 512, 6144, 256, 8, dict(seed=3)),
+    ("ragged", 37, 2056, 72, 3, dict(seed=8)),
+    ("no-shared", 5, 1024, 1024, 32, dict(seed=9, shared=False)),
+    ("e1", 3, 64, 1, 1, dict(seed=10)),
+]
+
+
+@pytest.mark.parametrize("name,T,H,E,k,kw", FUSED, ids=[f[0] for f in FUSED])
+def test_tail_fused(M, name, T, H, E, k, kw):
+    c = tail_case(T, H, E, k, router=False, logits=True, weights=False, **kw)
+    _check_fused(M, c, tag=name)
+
+
+@pytest.mark.parametrize("T", [2048, 8192])
+def test_tail_fused_full_size_sampled(M, T):
+    c = tail_case(T, 6144, 256, 8, router=False, logits=True, weights=False, seed=3)
+    rng = np.random.default_rng(T + 1)
+    tok = np.sort(rng.choice(T, 48, replace=False))
+    tok[0], tok[-1] = 0, T - 1
+    _check_fused(M, c, tok=tok, tag=f"T={T}")
+
+
+def test_tail_fused_without_route_outputs(M):
+    c = tail_case(16, 6144, 256, 8, router=False, logits=True, weights=False, seed=30)
+    a = _run_fused(M, c, want_route=False)
+    b = _run_fused(M, c, want_route=True)
+    assert a[2] is None and a[3] is None
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_tail_fused_matches_route_then_finalize_bitwise(M):
+    # same weights in, same kernel body: the fused launch equals route + finalize bit for bit
+    c = tail_case(64, 6144, 256, 8, router=False, logits=True, weights=False, seed=31)
+    ro, no, ids, w = _run_fused(M, c)
+    ids2, w2 = M.moe_topk_route(devf(c["logits"]), 8, c["scale"])
+    assert torch.equal(ids, ids2) and torch.equal(w, w2)
+    ro2, no2 = M.moe_finalize_add_rmsnorm(dev(c["rows"]), torch.from_numpy(c["map"]).cuda(), w2, dev(c["shared"]),
+                                          dev(c["residual"]), devf(c["gamma"]), c["eps"])
+    assert torch.equal(ro, ro2) and torch.equal(no, no2)
+
+
+# ---------------------------------------------------------------------------
+# the whole decode step: router -> route -> tail, and CUDA-graph replay
+# ---------------------------------------------------------------------------
+
+def _decode_step(M, g, c, fused):
+    logits = M.moe_router_logits_fp32(g["x"], g["w_gate"])
+    if fused:
+        ro, no, ids, w = M.moe_tail_fused(logits, c["k"], c["scale"], g["rows"], g["map"], g["shared"],
+                                          g["residual"], g["gamma"], c["eps"])
+    else:
+        ids, w = M.moe_topk_route(logits, c["k"], c["scale"])
+        ro, no = M.moe_finalize_add_rmsnorm(g["rows"], g["map"], w, g["shared"], g["residual"], g["gamma"], c["eps"])
+    return logits, ids, w, ro, no
+
+
+@pytest.mark.parametrize("T,fused", [(1, True), (4, False), (64, True), (64, False), (28, True)])
+def test_decode_chain(M, T, fused):
+    c = tail_case(T, 6144, 256, 8, seed=1, weights=False)
+    g = {"x": dev(c["x"]), "w_gate": dev(c["w_gate"]), "rows": dev(c["rows"]), "map": torch.from_numpy(c["map"]).cuda(),
+         "shared": dev(c["shared"]), "residual": dev(c["residual"]), "gamma": devf(c["gamma"])}
+    logits, ids, w, ro, no = _decode_step(M, g, c, fused)
+    L, A = O.router_logits(c["x"], c["w_gate"])
+    lg = logits.cpu().numpy().astype(np.float64)
+    ltol = 1e-5 * A
+    assert np.all(np.abs(lg - L) <= ltol)
+    # oracle route on its own logits; rows whose top-(k+1) order is decided by
+    # less than twice the logit tolerance may legitimately differ
+    rids, rw32, rw64 = O.topk_route(L.astype(np.float32), c["k"], c["scale"])
+    srt = -np.sort(-L, axis=1)[:, : c["k"] + 1]
+    gaps = np.abs(np.diff(srt, axis=1)).min(axis=1)
+    clear = gaps > 2 * ltol.max(axis=1) + 1e-6
+    ids = ids.cpu().numpy()
+    assert np.array_equal(ids[clear], rids[clear])
+    assert clear.mean() > 0.5
+    # weights: exp of logits that differ by <= ltol, plus the route tolerance
+    w = w.cpu().numpy().astype(np.float64)
+    wtol = route_weight_tol(L.astype(np.float32), rids, rw64) + rw64 * (np.exp(4 * ltol.max(axis=1, keepdims=True)) - 1)
+    assert np.all(np.abs(w[clear] - rw64[clear]) <= wtol[clear])
+    ref = O.finalize_add_rmsnorm(c["rows"], c["map"], rw32, c["shared"], None, c["residual"], c["gamma"], c["eps"])
+    rows = O.bf16_bits_to_f64(c["rows"])
+    extra = np.zeros_like(ref["r"])
+    for j in range(c["k"]):
+        extra += (wtol[:, j:j + 1] + rw64[:, j:j + 1] * 2.0 ** -24) * np.abs(rows[c["map"][:, j]])
+    cc = {**c, "shared": c["shared"][clear], "R": 0}
+    sub = {kk: (v[clear] if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] == T else v) for kk, v in ref.items()}
+    # the weight tolerance inherits the logit bound 1e-5 * sum|x w|, so this
+    # end-to-end check is wider than the per-step checks above
+    _check_tail(cc, sub, bits(ro)[clear], bits(no)[clear], extra_abs_r=extra[clear], tag=f"chain T={T}",
+                max_widened_frac=1.0)
+
+
+def test_cuda_graph_replay_matches_eager(M):
+    c = tail_case(64, 6144, 256, 8, seed=1, weights=False)
+    g = {"x": dev(c["x"]), "w_gate": dev(c["w_gate"]), "rows": dev(c["rows"]), "map": torch.from_numpy(c["map"]).cuda(),
+         "shared": dev(c["shared"]), "residual": dev(c["residual"]), "gamma": devf(c["gamma"])}
+    eager = _decode_step(M, g, c, True)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        _decode_step(M, g, c, True)  # warm up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        out = _decode_step(M, g, c, True)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager, out):
+        assert torch.equal(a, b)
+
+
+def test_nondefault_stream(M):
+    c = tail_case(12, 2048, 256, 8, router=False, seed=32)
+    ref = _oracle_tail(c)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        ro, no = M.moe_finalize_add_rmsnorm(dev(c["rows"]), torch.from_numpy(c["map"]).cuda(), devf(c["topk_w"]),
+                                            dev(c["shared"]), dev(c["residual"]), devf(c["gamma"]), c["eps"])
+    s.synchronize()
+    _check_tail(c, ref, bits(ro), bits(no), tag="stream")
+
+
+def test_empty_batch_launches_nothing(M):
+    x = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(16, 64, dtype=torch.bfloat16, device="cuda")
+    assert M.moe_router_logits_fp32(x, w).shape == (0, 16)
+    ids, wts = M.moe_topk_route(torch.empty(0, 16, device="cuda"), 4, 1.0)
+    assert ids.shape == (0, 4)
+    res = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    ro, no = M.moe_finalize_add_rmsnorm(None, None, None, None, res, torch.ones(64, device="cuda"), 1e-6)
+    assert ro.shape == (0, 64)
+
+
+def test_invalid_arguments_raise_and_launch_nothing(M):
+    res = torch.zeros(4, 60, dtype=torch.bfloat16, device="cuda")  # H % 8 != 0
+    with pytest.raises(M.MoeTailError) as ei:
+        M.moe_finalize_add_rmsnorm(None, None, None, None, res, torch.ones(60, device="cuda"), 1e-6)
+    assert ei.value.status == 2
+    x = torch.zeros(4, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(M.MoeTailError):
+        M.moe_topk_route(torch.zeros(4, 8, device="cuda"), 9, 1.0)
+    torch.cuda.synchronize()  # the context is healthy
+    assert M.moe_router_logits_fp32(x, torch.zeros(8, 64, dtype=torch.bfloat16, device="cuda")).abs().sum() == 0
