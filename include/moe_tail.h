@@ -63,6 +63,7 @@ typedef enum moe_status {
 
 /* Bits written (OR-ed) into the optional device error flag. */
 #define MOE_FLAG_BAD_INDEX 1 /* some map[t,j] was outside [0, n_rows) */
+#define MOE_FLAG_TIMEOUT 2   /* a bounded pipeline wait ran out (outputs of that launch are invalid) */
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* moe_status_string(int status);

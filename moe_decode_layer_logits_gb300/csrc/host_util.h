@@ -6,7 +6,7 @@
 #include <stdint.h>
 #include <math.h>
 
-#include "../../include/moe_tail.h"
+#include "moe_tail.h"  // include/ is on the include path
 
 namespace moe {
 
@@ -19,6 +19,15 @@ int sm_count();
 inline int launch_status() {
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Launch attribute that lets a kernel start while the previous kernel on the
+// stream finishes (the kernels wait on the dependency before touching memory).
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
 }
 
 // Largest number of tokens put on grid.y by one launch; the entry points loop

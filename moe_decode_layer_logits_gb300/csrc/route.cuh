@@ -2,48 +2,87 @@
 // equal logits in ascending expert order) and the routing weights
 // scale * softmax over the selected logits (vllm-project/vllm pull 62174,
 // Details: the router folds the routed scaling factor into the weights).
+//
+// Lane l holds the logits of experts l, l + 32, ... as order-preserving
+// integer keys in registers.  Each of the k rounds scans the lane's keys
+// (the first maximum wins, i.e. the lowest expert of the lane), then two
+// warp reductions pick the largest key and, among lanes holding it, the
+// lowest expert index; the winner clears its key.  Key 0 marks a taken or
+// padding slot: every finite logit has a key >= 1.
 #pragma once
 
 #include "common.cuh"
 
 namespace moe {
 
-// Orders (value, index) pairs: larger value first, then lower index.
-__device__ __forceinline__ bool route_better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
+// Monotone map float -> uint32 (a < b  <=>  key(a) < key(b)); -0 and +0 share
+// the key of +0, so they tie like equal floats.
+__device__ __forceinline__ uint32_t route_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u << 1) == 0u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// `row` points at the E logits of one token in shared memory.  Writes the k
-// selected expert ids and their weights to sel_id[0..k) / sel_w[0..k) (shared
-// memory).  Called by all 32 lanes of one warp; k <= 32, E <= 1024.
-__device__ __forceinline__ void warp_route(const float* row, int E, int k, float scale,
-                                           int* sel_id, float* sel_w) {
+__device__ __forceinline__ float route_unkey(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Load a token's logits row (global memory, E <= 32 * EPL) as keys; lane l
+// gets experts l, l + 32, ...  Split from the selection so that callers can
+// issue the loads early.
+template <int EPL>
+__device__ __forceinline__ void route_load_keys(const float* __restrict__ row, int E, uint32_t (&key)[EPL]) {
   const int lane = threadIdx.x & 31;
-  uint32_t taken = 0;  // bit s: element lane + 32 s already selected
-  float my_val = 0.f;  // lane j keeps the logit selected in round j
-  for (int round = 0; round < k; ++round) {
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-    for (int i = lane, s = 0; i < E; i += 32, ++s) {
-      if ((taken >> s) & 1u) continue;
-      const float v = row[i];
-      if (route_better(v, i, bv, bi)) { bv = v; bi = i; }
-    }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-      if (route_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+  for (int s = 0; s < EPL; ++s) {
+    const int i = lane + 32 * s;
+    key[s] = i < E ? route_key(__ldg(row + i)) : 0u;
+  }
+}
+
+// Select the top k (1 <= k <= min(E, 32)) of the keys held by the warp and
+// weight them.  All 32 lanes call this; lane j < k receives the j-th
+// selected expert in `id` and its weight in `w`.  Consumes `key`.
+template <int EPL>
+__device__ __forceinline__ void route_select(uint32_t (&key)[EPL], int k, float scale, int& id, float& w) {
+  const int lane = threadIdx.x & 31;
+  uint32_t my_key = 0u;
+  int my_id = 0;
+  for (int round = 0; round < k; ++round) {
+    uint32_t bk = 0u;
+    int bs = 0;
+#pragma unroll
+    for (int s = 0; s < EPL; ++s) {
+      if (key[s] > bk) { bk = key[s]; bs = s; }
     }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == round) my_val = bv;
-    if (lane == 0) sel_id[round] = bi;
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, bk);
+    const uint32_t cand = bk == m ? static_cast<uint32_t>(lane + 32 * bs) : 0xFFFFFFFFu;
+    const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, cand);
+    if (static_cast<int>(win & 31u) == lane) {
+      const int ws = static_cast<int>(win >> 5);
+#pragma unroll
+      for (int s = 0; s < EPL; ++s) {
+        if (s == ws) key[s] = 0u;
+      }
+    }
+    if (lane == round) { my_key = m; my_id = static_cast<int>(win); }
   }
   // weights: exp relative to the largest selected logit, summed over lanes
-  const float top = __shfl_sync(0xFFFFFFFFu, my_val, 0);
-  const float e = lane < k ? expf(my_val - top) : 0.f;
+  const float val = route_unkey(my_key);
+  const float top = __shfl_sync(0xFFFFFFFFu, val, 0);
+  const float e = lane < k ? expf(val - top) : 0.f;
   const float sum = warp_sum(e);
-  if (lane < k) sel_w[lane] = (scale * e) / sum;
+  id = my_id;
+  w = (scale * e) / sum;
+}
+
+// Both phases for one token row.
+template <int EPL>
+__device__ __forceinline__ void warp_route(const float* __restrict__ row, int E, int k, float scale,
+                                           int& id, float& w) {
+  uint32_t key[EPL];
+  route_load_keys<EPL>(row, E, key);
+  route_select<EPL>(key, k, scale, id, w);
 }
 
 }  // namespace moe

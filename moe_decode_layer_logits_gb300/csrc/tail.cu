@@ -44,15 +44,15 @@ struct TailParams {
 
 constexpr int kMaxThreads = 256;  // per CTA; VPT <= 4 covers 1024 vectors (16 KB of a row)
 
-template <int VPT, int KB, bool ROUTE>
+// EPL > 0: route the token from its logits first (E <= 32 * EPL).
+template <int VPT, int KB, int EPL>
 __global__ void __launch_bounds__(kMaxThreads)
 tail_kernel(const TailParams p) {
+  constexpr bool ROUTE = EPL > 0;
   __shared__ int map_s[MOE_MAX_K];
   __shared__ float w_s[MOE_MAX_K];
-  __shared__ int id_s[MOE_MAX_K];
   __shared__ float red[33];
   __shared__ float cluster_slot;
-  extern __shared__ float logit_s[];  // E floats when ROUTE
 
   const int t = blockIdx.y;
   const int tid = threadIdx.x;
@@ -66,6 +66,9 @@ tail_kernel(const TailParams p) {
   const int64_t row_off = static_cast<int64_t>(t) * p.H;
   const int k = p.k;
 
+  allow_dependent_launch();
+  grid_dependency_wait();
+
   // -- slot table: map entries (checked) and, without routing, the weights
   if (tid < k) {
     int m = p.map[static_cast<int64_t>(t) * k + tid];
@@ -75,10 +78,6 @@ tail_kernel(const TailParams p) {
     }
     map_s[tid] = m;
     if (!ROUTE) w_s[tid] = p.topk_w[static_cast<int64_t>(t) * k + tid];
-  }
-  if (ROUTE) {
-    const float* src = p.logits + static_cast<int64_t>(t) * p.E;
-    for (int i = tid; i < p.E; i += nthr) logit_s[i] = src[i];
   }
   __syncthreads();
 
@@ -121,13 +120,20 @@ tail_kernel(const TailParams p) {
     }
     if (ROUTE && jb == 0) {
       // route the token while the first batch of rows is in flight
-      if (tid < 32) warp_route(logit_s, p.E, k, p.scale, id_s, w_s);
-      __syncthreads();
-      if (rank == 0 && tid < k) {
-        const int64_t o = static_cast<int64_t>(t) * k + tid;
-        if (p.ids_out) p.ids_out[o] = id_s[tid];
-        if (p.w_out) p.w_out[o] = w_s[tid];
+      if (tid < 32) {
+        int id;
+        float w;
+        warp_route<(EPL > 0 ? EPL : 1)>(p.logits + static_cast<int64_t>(t) * p.E, p.E, k, p.scale, id, w);
+        if (tid < k) {
+          w_s[tid] = w;
+          if (rank == 0) {
+            const int64_t o = static_cast<int64_t>(t) * k + tid;
+            if (p.ids_out) p.ids_out[o] = id;
+            if (p.w_out) p.w_out[o] = w;
+          }
+        }
       }
+      __syncthreads();
     }
 #pragma unroll
     for (int j = 0; j < KB; ++j) {
@@ -224,6 +230,273 @@ tail_kernel(const TailParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// Large batches: a persistent kernel fed by bulk copies (TMA).
+//
+// One CTA per SM walks the tokens t = blockIdx.x, + gridDim.x, ...
+//  - warp 0 (producer): lane j copies slot j's expert-row piece (then the
+//    shared, partial and residual pieces) of one chunk of H into a ring of
+//    shared-memory stages with cp.async.bulk, counted on the stage's "full"
+//    mbarrier; the next token's map entries are prefetched while copies fly;
+//  - warp 1 (weights): per token, the routing weights -- loaded, or routed
+//    from the logits (router-less variant) -- into a ring of token slots, up
+//    to kWRing tokens ahead of the consumers; unusable map entries get 0;
+//  - warps 2..9 (consumers): FP32 accumulation in the same order as
+//    tail_kernel, residual_out stored per chunk, the token's r kept in
+//    registers across chunks until the sum of squares is reduced, then the
+//    normalised row stored.  Each consumer warp releases a stage ("empty")
+//    after reading it and a token slot after the token's last chunk.
+// Every wait is bounded: one that runs out sets MOE_FLAG_TIMEOUT and a
+// shared abort flag, after which nobody waits any more and the producer only
+// drains the copies it has in flight.
+// ---------------------------------------------------------------------------
+
+constexpr int kStreamConsumerWarps = 8;
+constexpr int kStreamConsumers = 32 * kStreamConsumerWarps;
+constexpr int kStreamThreads = 64 + kStreamConsumers;
+constexpr int kStreamMaxStages = 8;
+constexpr int kWRing = 4;
+constexpr int kStreamSmemBudget = 200 * 1024;
+constexpr uint32_t kProbeHintNs = 1000;
+constexpr int kMaxProbes = 1 << 21;  // ~2 s of probes per wait before giving up
+
+struct StreamShape {
+  int chunk;        // row elements per stage (multiple of 8)
+  int nchunks;      // chunks per row
+  int nstages;      // stages in the ring
+  int rows;         // row pieces per stage: k slots, shared, R partials, residual
+  int stage_bytes;  // rows * chunk * 2 rounded up to 128
+};
+
+__device__ __forceinline__ bool stream_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                            int32_t* err_flag) {
+  for (int it = 0; it < kMaxProbes; ++it) {
+    if (mbar_try_wait(bar, parity, kProbeHintNs)) return true;
+    if (*abort_flag) return false;
+  }
+  *abort_flag = 1;
+  if (err_flag) atomicOr(err_flag, MOE_FLAG_TIMEOUT);
+  return false;
+}
+
+// Checked map entry of slot `lane` of token t, or -1 (flagged) if unusable.
+__device__ __forceinline__ int stream_map_entry(const TailParams& p, int64_t t, int lane) {
+  int m = p.map[t * p.k + lane];
+  if (m < 0 || static_cast<int64_t>(m) >= p.n_rows) {
+    if (p.err_flag) atomicOr(p.err_flag, MOE_FLAG_BAD_INDEX);
+    m = -1;
+  }
+  return m;
+}
+
+template <int VPT, int EPL>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
+  constexpr bool ROUTE = EPL > 0;
+  constexpr int KEYS = EPL > 0 ? EPL : 1;
+  extern __shared__ __align__(128) unsigned char stage_mem[];
+  __shared__ uint64_t full_bar[kStreamMaxStages];
+  __shared__ uint64_t empty_bar[kStreamMaxStages];
+  __shared__ uint64_t wfull_bar[kWRing];
+  __shared__ uint64_t wempty_bar[kWRing];
+  __shared__ float w_ring[kWRing][MOE_MAX_K];
+  __shared__ float red[2][kStreamConsumerWarps];
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int k = p.k, H = p.H, nvec = H >> 3;
+  const int G = static_cast<int>(gridDim.x);
+  const int ntok = (T - static_cast<int>(blockIdx.x) + G - 1) / G;
+  volatile int* abort_v = &abort_flag;
+
+  if (tid == 0) {
+    for (int s = 0; s < sh.nstages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kStreamConsumerWarps);
+    }
+    for (int s = 0; s < kWRing; ++s) {
+      mbar_init(&wfull_bar[s], 1);
+      mbar_init(&wempty_bar[s], kStreamConsumerWarps);
+    }
+    abort_flag = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+  allow_dependent_launch();
+  grid_dependency_wait();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = l2_evict_first_policy();
+    int row_cur = -1, row_nxt = -1;
+    if (ntok > 0 && lane < k) row_cur = stream_map_entry(p, blockIdx.x, lane);
+    int issued = 0;
+    for (int i = 0; i < ntok && !*abort_v; ++i) {
+      const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(i) * G;
+      const int64_t roff = t * H;
+      for (int c = 0; c < sh.nchunks; ++c) {
+        const int u = i * sh.nchunks + c, s = u % sh.nstages, n = u / sh.nstages;
+        if (n > 0 && !stream_wait(&empty_bar[s], (n - 1) & 1, abort_v, p.err_flag)) break;
+        const int c0 = c * sh.chunk;
+        const int clen = min(sh.chunk, H - c0);
+        if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(sh.rows * clen * 2));
+        __syncwarp();
+        unsigned char* st = stage_mem + static_cast<size_t>(s) * sh.stage_bytes;
+        for (int l = lane; l < sh.rows; l += 32) {
+          const uint16_t* src;
+          if (l < k) {
+            // an unusable slot reads the residual row instead; its weight is 0
+            src = row_cur >= 0 ? p.rows + static_cast<int64_t>(row_cur) * H : p.residual + roff;
+          } else if (p.shared && l == k) {
+            src = p.shared + roff;
+          } else if (l < sh.rows - 1) {
+            const int r = l - k - (p.shared ? 1 : 0);
+            src = p.partials + static_cast<int64_t>(r) * p.partial_stride + roff;
+          } else {
+            src = p.residual + roff;
+          }
+          bulk_copy_g2s(st + static_cast<size_t>(l) * sh.chunk * 2, src + c0, static_cast<uint32_t>(clen * 2),
+                        &full_bar[s], pol);
+        }
+        issued = u + 1;
+        if (c == 0 && i + 1 < ntok && lane < k) row_nxt = stream_map_entry(p, t + G, lane);
+      }
+      row_cur = row_nxt;
+    }
+    // drain: no copy may land after this CTA exits
+    if (lane == 0) {
+      for (int u = issued > sh.nstages ? issued - sh.nstages : 0; u < issued; ++u) {
+        for (int it = 0; it < kMaxProbes; ++it)
+          if (mbar_try_wait(&full_bar[u % sh.nstages], (u / sh.nstages) & 1, kProbeHintNs)) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ weights
+    uint32_t keys[KEYS], keys_nxt[KEYS];
+    float w_nxt = 0.f;
+    int ok_nxt = 0;
+    auto fetch = [&](int64_t t, uint32_t (&kk)[KEYS], float& w, int& ok) {
+      if (lane < k) {
+        ok = stream_map_entry(p, t, lane) >= 0;
+        if (!ROUTE) w = p.topk_w[t * k + lane];
+      }
+      if (ROUTE) route_load_keys<KEYS>(p.logits + t * p.E, p.E, kk);
+    };
+    if (ntok > 0) fetch(blockIdx.x, keys, w_nxt, ok_nxt);
+    for (int i = 0; i < ntok && !*abort_v; ++i) {
+      const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(i) * G;
+      float w = w_nxt;
+      const int ok = ok_nxt;
+      if (ROUTE) {
+#pragma unroll
+        for (int e = 0; e < KEYS; ++e) keys_nxt[e] = keys[e];
+      }
+      if (i + 1 < ntok) fetch(t + G, keys, w_nxt, ok_nxt);  // next token's loads in flight
+      if (ROUTE) {
+        int id;
+        route_select<KEYS>(keys_nxt, k, p.scale, id, w);
+        if (lane < k) {
+          if (p.ids_out) p.ids_out[t * k + lane] = id;
+          if (p.w_out) p.w_out[t * k + lane] = w;
+        }
+      }
+      const int slot = i % kWRing, n = i / kWRing;
+      if (n > 0 && !stream_wait(&wempty_bar[slot], (n - 1) & 1, abort_v, p.err_flag)) break;
+      if (lane < k) w_ring[slot][lane] = ok ? w : 0.f;
+      __syncwarp();  // the weights are published by lane 0's arrive
+      if (lane == 0) mbar_arrive(&wfull_bar[slot]);
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int ct = tid - 64, cw = warp - 2;
+    const int ncv = sh.chunk >> 3;  // vectors per chunk
+    float rr[VPT][8];
+    for (int i = 0; i < ntok; ++i) {
+      const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(i) * G;
+      const int64_t roff = t * H;
+      const int slot = i % kWRing;
+      if (!*abort_v) stream_wait(&wfull_bar[slot], (i / kWRing) & 1, abort_v, p.err_flag);
+      float ss = 0.f;
+      for (int c = 0; c < sh.nchunks; ++c) {
+        const int u = i * sh.nchunks + c, s = u % sh.nstages, n = u / sh.nstages;
+        if (!*abort_v) stream_wait(&full_bar[s], n & 1, abort_v, p.err_flag);
+        const unsigned char* st = stage_mem + static_cast<size_t>(s) * sh.stage_bytes;
+        const int vb = c * ncv, ve = min(nvec, vb + ncv);
+        const int pitch = sh.chunk * 2;
+#pragma unroll
+        for (int m = 0; m < VPT; ++m) {
+          const int v = ct + m * kStreamConsumers;
+          if (v < vb || v >= ve) continue;
+          const int off = (v - vb) * 16;
+          float acc[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll 4
+          for (int j = 0; j < k; ++j) {
+            const float w = w_ring[slot][j];
+            float f[8];
+            unpack8(lds16(st + j * pitch + off), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, f[e], acc[e]);
+          }
+          int l = k;
+          if (p.shared) {
+            float f[8];
+            unpack8(lds16(st + l * pitch + off), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] += f[e];
+            ++l;
+          }
+          for (int r = 0; r < p.R; ++r, ++l) {
+            float f[8];
+            unpack8(lds16(st + l * pitch + off), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] += f[e];
+          }
+          float f[8];
+          unpack8(lds16(st + (sh.rows - 1) * pitch + off), f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            rr[m][e] = f[e] + acc[e];
+            ss = fmaf(rr[m][e], rr[m][e], ss);
+          }
+          uint4 o;
+          o.x = pack_bf16x2(rr[m][0], rr[m][1]);
+          o.y = pack_bf16x2(rr[m][2], rr[m][3]);
+          o.z = pack_bf16x2(rr[m][4], rr[m][5]);
+          o.w = pack_bf16x2(rr[m][6], rr[m][7]);
+          st16(p.residual_out + roff + static_cast<int64_t>(v) * 8, o);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+      }
+      if (lane == 0) mbar_arrive(&wempty_bar[slot]);
+      // sum of squares over the consumer warps, added in warp order
+      ss = warp_sum(ss);
+      if (lane == 0) red[i & 1][cw] = ss;
+      named_barrier(1, kStreamConsumers);
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < kStreamConsumerWarps; ++w) tot += red[i & 1][w];
+      const float inv = rsqrtf(tot / static_cast<float>(H) + p.eps);
+#pragma unroll
+      for (int m = 0; m < VPT; ++m) {
+        const int v = ct + m * kStreamConsumers;
+        if (v >= nvec) continue;
+        const float4* g4 = reinterpret_cast<const float4*>(p.gamma + static_cast<int64_t>(v) * 8);
+        const float4 g0 = __ldg(g4), g1 = __ldg(g4 + 1);
+        uint4 o;
+        o.x = pack_bf16x2(rr[m][0] * inv * g0.x, rr[m][1] * inv * g0.y);
+        o.y = pack_bf16x2(rr[m][2] * inv * g0.z, rr[m][3] * inv * g0.w);
+        o.z = pack_bf16x2(rr[m][4] * inv * g1.x, rr[m][5] * inv * g1.y);
+        o.w = pack_bf16x2(rr[m][6] * inv * g1.z, rr[m][7] * inv * g1.w);
+        st16(p.normed_out + roff + static_cast<int64_t>(v) * 8, o);
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
 // Launch configuration: a deterministic function of (T, H, SM count).
 // ---------------------------------------------------------------------------
 
@@ -249,32 +522,103 @@ static TailLaunch choose_tail_launch(int64_t T, int H, int nsm) {
   return {cs, vpt, threads};
 }
 
-template <int VPT, bool ROUTE>
-static cudaError_t launch_tail_v(const TailParams& p, int T, const TailLaunch& L, size_t smem,
-                                 cudaStream_t stream) {
+template <int VPT, int EPL>
+static cudaError_t launch_tail_v(const TailParams& p, int T, const TailLaunch& L, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.cs, T, 1);
   cfg.blockDim = dim3(L.threads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  int nattr = 0;
+  cudaLaunchAttribute attr[2];
+  attr[0] = pdl_attribute();
+  int nattr = 1;
   if (L.cs > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = L.cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    nattr = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = L.cs;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    nattr = 2;
   }
   cfg.attrs = attr;
   cfg.numAttrs = nattr;
-  return cudaLaunchKernelEx(&cfg, tail_kernel<VPT, 8, ROUTE>, p);
+  return cudaLaunchKernelEx(&cfg, tail_kernel<VPT, 8, EPL>, p);
+}
+
+template <int EPL>
+static cudaError_t launch_tail_e(const TailParams& q, int Tc, const TailLaunch& L, cudaStream_t stream) {
+  switch (L.vpt) {
+    case 1: return launch_tail_v<1, EPL>(q, Tc, L, stream);
+    case 2: return launch_tail_v<2, EPL>(q, Tc, L, stream);
+    case 3: return launch_tail_v<3, EPL>(q, Tc, L, stream);
+    default: return launch_tail_v<4, EPL>(q, Tc, L, stream);
+  }
+}
+
+// Stage geometry of the stream kernel: the fewest chunks per row that leave
+// room for at least three stages within the shared-memory budget.
+static bool stream_shape(int H, int rows, StreamShape& sh) {
+  for (int nch = 1; nch <= 64; ++nch) {
+    const int chunk = ((H + nch - 1) / nch + 7) / 8 * 8;
+    const int stage = (rows * chunk * 2 + 127) / 128 * 128;
+    const int ns = kStreamSmemBudget / stage;
+    if (ns >= 3) {
+      sh.chunk = chunk;
+      sh.nchunks = (H + chunk - 1) / chunk;
+      sh.nstages = ns < kStreamMaxStages ? ns : kStreamMaxStages;
+      sh.rows = rows;
+      sh.stage_bytes = stage;
+      return true;
+    }
+  }
+  return false;
+}
+
+template <int VPT, int EPL>
+static cudaError_t launch_stream_v(const TailParams& p, int T, const StreamShape& sh, int grid,
+                                   cudaStream_t stream) {
+  static bool smem_opt_in[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (dev >= 0 && dev < 64 && !smem_opt_in[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(tail_stream_kernel<VPT, EPL>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamSmemBudget);
+    if (e != cudaSuccess) return e;
+    smem_opt_in[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kStreamThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(sh.nstages) * sh.stage_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tail_stream_kernel<VPT, EPL>, p, T, sh);
+}
+
+template <int EPL>
+static cudaError_t launch_stream_e(const TailParams& p, int T, const StreamShape& sh, int grid, int vpt,
+                                   cudaStream_t stream) {
+  switch (vpt) {
+    case 1: return launch_stream_v<1, EPL>(p, T, sh, grid, stream);
+    case 2: return launch_stream_v<2, EPL>(p, T, sh, grid, stream);
+    case 3: return launch_stream_v<3, EPL>(p, T, sh, grid, stream);
+    default: return launch_stream_v<4, EPL>(p, T, sh, grid, stream);
+  }
+}
+
+// The stream kernel takes batches of at least two tokens per SM whose rows fit
+// four vectors per consumer thread.
+static bool use_stream(int64_t T, int H, int rows, int nsm, StreamShape& sh) {
+  return T >= 2 * static_cast<int64_t>(nsm) && H / 8 <= 4 * kStreamConsumers && stream_shape(H, rows, sh);
 }
 
 template <bool ROUTE>
 static int launch_tail(TailParams p, int64_t T, cudaStream_t stream) {
   const int nsm = sm_count();
-  const size_t smem = ROUTE ? sizeof(float) * static_cast<size_t>(p.E) : 0;
+  StreamShape sh;
+  const int rows = p.k + (p.shared ? 1 : 0) + p.R + 1;
+  const bool stream_path = use_stream(T, p.H, rows, nsm, sh);
   for (int64_t t0 = 0; t0 < T; t0 += kMaxGridY) {
     const int Tc = static_cast<int>(T - t0 < kMaxGridY ? T - t0 : kMaxGridY);
     TailParams q = p;
@@ -289,13 +633,18 @@ static int launch_tail(TailParams p, int64_t T, cudaStream_t stream) {
     if (q.logits) q.logits += t0 * p.E;
     if (q.ids_out) q.ids_out += t0 * p.k;
     if (q.w_out) q.w_out += t0 * p.k;
-    const TailLaunch L = choose_tail_launch(T, p.H, nsm);
     cudaError_t e;
-    switch (L.vpt) {
-      case 1: e = launch_tail_v<1, ROUTE>(q, Tc, L, smem, stream); break;
-      case 2: e = launch_tail_v<2, ROUTE>(q, Tc, L, smem, stream); break;
-      case 3: e = launch_tail_v<3, ROUTE>(q, Tc, L, smem, stream); break;
-      default: e = launch_tail_v<4, ROUTE>(q, Tc, L, smem, stream); break;
+    if (stream_path) {
+      const int grid = Tc < nsm ? Tc : nsm;
+      const int vpt = (p.H / 8 + kStreamConsumers - 1) / kStreamConsumers;
+      if (!ROUTE) e = launch_stream_e<0>(q, Tc, sh, grid, vpt, stream);
+      else if (p.E <= 256) e = launch_stream_e<8>(q, Tc, sh, grid, vpt, stream);
+      else e = launch_stream_e<32>(q, Tc, sh, grid, vpt, stream);
+    } else {
+      const TailLaunch L = choose_tail_launch(T, p.H, nsm);
+      if (!ROUTE) e = launch_tail_e<0>(q, Tc, L, stream);
+      else if (p.E <= 256) e = launch_tail_e<8>(q, Tc, L, stream);
+      else e = launch_tail_e<32>(q, Tc, L, stream);
     }
     if (e != cudaSuccess) {
       (void)cudaGetLastError();

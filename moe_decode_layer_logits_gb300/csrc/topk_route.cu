@@ -7,25 +7,35 @@ namespace moe {
 
 constexpr int kRouteWarps = 8;  // tokens per CTA
 
+template <int EPL>
 __global__ void __launch_bounds__(kRouteWarps * 32)
-topk_route_kernel(const float* __restrict__ logits, int32_t* __restrict__ ids,
-                  float* __restrict__ wts, int T, int E, int k, float scale) {
-  extern __shared__ float smem[];
+topk_route_kernel(const float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ wts,
+                  int T, int E, int k, float scale) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* row = smem + warp * E;
-  int* sel_id = reinterpret_cast<int*>(smem + kRouteWarps * E) + warp * 2 * MOE_MAX_K;
-  float* sel_w = reinterpret_cast<float*>(sel_id + MOE_MAX_K);
   const int t = blockIdx.x * kRouteWarps + warp;
-  if (t >= T) return;  // whole warp leaves together; no block-wide barrier below
-  const float* src = logits + static_cast<int64_t>(t) * E;
-  for (int i = lane; i < E; i += 32) row[i] = src[i];
-  __syncwarp();
-  warp_route(row, E, k, scale, sel_id, sel_w);
-  __syncwarp();
+  allow_dependent_launch();
+  grid_dependency_wait();
+  if (t >= T) return;  // whole warp leaves together; the kernel has no block barrier
+  int id;
+  float w;
+  warp_route<EPL>(logits + static_cast<int64_t>(t) * E, E, k, scale, id, w);
   if (lane < k) {
-    ids[static_cast<int64_t>(t) * k + lane] = sel_id[lane];
-    wts[static_cast<int64_t>(t) * k + lane] = sel_w[lane];
+    ids[static_cast<int64_t>(t) * k + lane] = id;
+    wts[static_cast<int64_t>(t) * k + lane] = w;
   }
+}
+
+template <int EPL>
+static cudaError_t launch_route(const float* logits, int32_t* ids, float* w, int T, int E, int k, float scale,
+                         cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((T + kRouteWarps - 1) / kRouteWarps), 1, 1);
+  cfg.blockDim = dim3(kRouteWarps * 32, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk_route_kernel<EPL>, logits, ids, w, T, E, k, scale);
 }
 
 }  // namespace moe
@@ -40,13 +50,24 @@ extern "C" int moe_topk_route(const float* logits, int32_t* topk_ids, float* top
   if (T == 0) return MOE_OK;
   if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
   if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4)) return MOE_ERR_MISALIGNED;
-  const size_t smem = sizeof(float) * kRouteWarps * (E + 2 * MOE_MAX_K);
-  const int64_t per_launch = kMaxGridY * kRouteWarps * 1024;  // grid.x limit is far away
+  const int64_t per_launch = static_cast<int64_t>(1) << 30;  // keeps grid.x in range
   for (int64_t t0 = 0; t0 < T; t0 += per_launch) {
     const int Tc = static_cast<int>(T - t0 < per_launch ? T - t0 : per_launch);
-    const unsigned grid = static_cast<unsigned>((Tc + kRouteWarps - 1) / kRouteWarps);
-    topk_route_kernel<<<grid, kRouteWarps * 32, smem, stream>>>(
-        logits + t0 * E, topk_ids + t0 * k, topk_w + t0 * k, Tc, static_cast<int>(E), k, routed_scale);
+    const float* lg = logits + t0 * E;
+    int32_t* ip = topk_ids + t0 * k;
+    float* wp = topk_w + t0 * k;
+    const int Ei = static_cast<int>(E);
+    cudaError_t e;
+    if (E <= 32) e = launch_route<1>(lg, ip, wp, Tc, Ei, k, routed_scale, stream);
+    else if (E <= 64) e = launch_route<2>(lg, ip, wp, Tc, Ei, k, routed_scale, stream);
+    else if (E <= 128) e = launch_route<4>(lg, ip, wp, Tc, Ei, k, routed_scale, stream);
+    else if (E <= 256) e = launch_route<8>(lg, ip, wp, Tc, Ei, k, routed_scale, stream);
+    else if (E <= 512) e = launch_route<16>(lg, ip, wp, Tc, Ei, k, routed_scale, stream);
+    else e = launch_route<32>(lg, ip, wp, Tc, Ei, k, routed_scale, stream);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
     const int st = launch_status();
     if (st != MOE_OK) return st;
   }

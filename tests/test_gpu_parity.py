@@ -185,6 +185,13 @@ FIN = [  # name, T, H, E, k, extra kwargs
     ("h16384", 3, 16384, 16, 8, dict(seed=13)),
     ("h65536", 2, 65536, 16, 4, dict(seed=14)),
     ("t300", 300, 2048, 16, 8, dict(seed=15)),
+    # batches of >= 2 tokens per SM take the persistent bulk-copy kernel
+    ("stream-ragged-h", 400, 2056, 72, 5, dict(seed=16)),
+    ("stream-mixed", 333, 6144, 256, 3, dict(seed=17, R=2)),
+    ("stream-42-pieces", 310, 512, 64, 32, dict(seed=18, R=8)),
+    ("stream-h8192", 320, 8192, 64, 8, dict(seed=19, s=4.0)),
+    ("stream-shared-only", 304, 1024, 16, 0, dict(seed=20)),
+    ("stream-padded", 350, 768, 16, 8, dict(seed=21, n_rows=4000)),
 ]
 
 
@@ -217,8 +224,9 @@ def test_finalize_residual_out_may_alias_residual(M):
     _check_tail(c, ref, ro, no, tag="alias")
 
 
-def test_finalize_bad_index_sets_flag_and_reads_zero(M):
-    c = tail_case(6, 1024, 16, 4, router=False, seed=21)
+@pytest.mark.parametrize("T", [6, 400])
+def test_finalize_bad_index_sets_flag_and_reads_zero(M, T):
+    c = tail_case(T, 1024, 16, 4, router=False, seed=21)
     n = c["rows"].shape[0]
     c["map"] = c["map"].copy()
     c["map"][1, 2] = n          # one past the end
@@ -300,6 +308,8 @@ FUSED = [  # name, T, H, E, k, kw
     ("ragged", 37, 2056, 72, 3, dict(seed=8)),
     ("no-shared", 5, 1024, 1024, 32, dict(seed=9, shared=False)),
     ("e1", 3, 64, 1, 1, dict(seed=10)),
+    ("stream-e1024", 320, 1024, 1024, 32, dict(seed=11)),
+    ("stream-ragged", 400, 2056, 72, 3, dict(seed=12, shared=False)),
 ]
 
 
