@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--min-timed-s", type=float, default=1.0,
                     help="repeat the K-step timed region until this much time is covered")
+    ap.add_argument("--ncu-case", choices=["decode", "prefill"], default=None,
+                    help="run a small fixed case for an ncu capture and exit (no timing, no JSON)")
     return ap.parse_args()
 
 
@@ -376,31 +378,58 @@ def run_ours(args):
 
 
 def run_e2e(torch, M, layers, stream, K, warmup):
-    """Same step, host buffers: H2D of the step's activations from pinned host
-    memory, the three C-ABI calls, D2H of both outputs; timed with events."""
+    """Same step, host buffers: every step copies its activations (x, expert
+    rows, map, shared, residual) from one pinned host staging buffer to the
+    device in a single copy, makes the three C-ABI calls, and copies both
+    outputs back to a pinned host buffer in a single copy; timed with events.
+    Gate weights and gamma stay resident (model parameters)."""
     d0 = layers[0]
     names_in = ["x", "rows", "map", "shared", "residual"]
-    host_in = {n: torch.empty_like(d0[n], device="cpu").pin_memory() for n in names_in}
+    names_out = ["residual_out", "normed_out"]
+
+    def layout(names):
+        offs, o = {}, 0
+        for n in names:
+            offs[n] = o
+            o += (d0[n].numel() * d0[n].element_size() + 255) // 256 * 256
+        return offs, o
+
+    offs_in, n_in = layout(names_in)
+    offs_out, n_out = layout(names_out)
+
+    def views(buf, offs, names):
+        v = {}
+        for n in names:
+            nb = d0[n].numel() * d0[n].element_size()
+            v[n] = buf[offs[n]:offs[n] + nb].view(d0[n].dtype).view(d0[n].shape)
+        return v
+
+    host_in = torch.empty(n_in, dtype=torch.uint8).pin_memory()
+    hv = views(host_in, offs_in, names_in)
     for n in names_in:
-        host_in[n].copy_(d0[n].cpu())
-    host_out = {n: torch.empty_like(d0[n], device="cpu").pin_memory() for n in ["residual_out", "normed_out"]}
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        hv[n].copy_(d0[n].cpu())
+    host_out = torch.empty(n_out, dtype=torch.uint8).pin_memory()
+    nsets = 8
+    dev_in = [torch.empty(n_in, dtype=torch.uint8, device=d0["x"].device) for _ in range(nsets)]
+    dev_out = [torch.empty(n_out, dtype=torch.uint8, device=d0["x"].device) for _ in range(nsets)]
+    dvi = [views(b, offs_in, names_in) for b in dev_in]
+    dvo = [views(b, offs_out, names_out) for b in dev_out]
+    h2d = sum(hv[n].numel() * hv[n].element_size() for n in names_in)
+    d2h = sum(d0[n].numel() * d0[n].element_size() for n in names_out)
     s = stream.cuda_stream
     n_steps = max(1, min(K, 750))
 
     def one(i):
         d = layers[i % len(layers)]
+        a, o = dvi[i % nsets], dvo[i % nsets]
         with torch.cuda.stream(stream):
-            for n in names_in:
-                d[n].copy_(host_in[n], non_blocking=True)
-            M.moe_router_logits_fp32(d["x"], d["w_gate"], logits_out=d["logits"], stream=s)
+            dev_in[i % nsets].copy_(host_in, non_blocking=True)
+            M.moe_router_logits_fp32(a["x"], d["w_gate"], logits_out=d["logits"], stream=s)
             M.moe_topk_route(d["logits"], K_DEC, SCALE, topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
-            M.moe_finalize_add_rmsnorm(d["rows"], d["map"], d["topk_w"], d["shared"], d["residual"], d["gamma"],
-                                       d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"],
+            M.moe_finalize_add_rmsnorm(a["rows"], a["map"], d["topk_w"], a["shared"], a["residual"], d["gamma"],
+                                       d["eps"], residual_out=o["residual_out"], normed_out=o["normed_out"],
                                        stream=s)
-            host_out["residual_out"].copy_(d["residual_out"], non_blocking=True)
-            host_out["normed_out"].copy_(d["normed_out"], non_blocking=True)
+            host_out.copy_(dev_out[i % nsets], non_blocking=True)
 
     for i in range(max(warmup, 3)):
         one(i)
@@ -414,7 +443,9 @@ def run_e2e(torch, M, layers, stream, K, warmup):
     e1.synchronize()
     us = e0.elapsed_time(e1) * 1000.0 / n_steps
     return {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": n_steps, "what": "pinned host -> device copies, 3 C-ABI calls, device -> pinned host copies"}
+            "steps": n_steps,
+            "what": "one pinned host -> device copy of the step's activations, 3 C-ABI calls, "
+                    "one device -> pinned host copy of both outputs"}
 
 
 def run_sweep(torch, M, stream, l2, peak):
@@ -554,8 +585,40 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_ncu_case(case):
+    """Small cases for ncu captures (a few hundred MB, more than the L2):
+    decode -- 12 layers at T=64 (162 MB), router -> route -> finalize on each
+    layer, twice; prefill -- 2 sets at T=2048 (605 MB), route, finalize and the
+    router-less fused tail on each set, twice."""
+    import torch
+    import moe_decode_layer_logits_gb300 as M
+    from moe_decode_layer_logits_gb300.inputs import device_layer
+    M.lib()
+    if case == "decode":
+        sets = [device_layer(T_DEC, H_DEC, E_DEC, K_DEC, seed=i, scale=SCALE) for i in range(12)]
+    else:
+        sets = [device_layer(2048, H_DEC, E_DEC, K_DEC, seed=100 + i, scale=SCALE, router=False, logits=True)
+                for i in range(2)]
+    torch.cuda.synchronize()
+    for _ in range(2):
+        for d in sets:
+            if case == "decode":
+                M.moe_router_logits_fp32(d["x"], d["w_gate"], logits_out=d["logits"])
+            M.moe_topk_route(d["logits"], K_DEC, SCALE, topk_ids=d["topk_ids"], topk_w=d["topk_w"])
+            M.moe_finalize_add_rmsnorm(d["rows"], d["map"], d["topk_w"], d["shared"], d["residual"], d["gamma"],
+                                       d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"])
+            if case == "prefill":
+                M.moe_tail_fused(d["logits"], K_DEC, SCALE, d["rows"], d["map"], d["shared"], d["residual"],
+                                 d["gamma"], d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"],
+                                 want_route=False)
+    torch.cuda.synchronize()
+
+
 def main():
     args = parse_args()
+    if args.ncu_case:
+        run_ncu_case(args.ncu_case)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -86,18 +86,35 @@ __device__ __forceinline__ float block_sum(float v, float* scratch) {
   return scratch[32];
 }
 
-// Sum of one float per CTA over the thread-block cluster through distributed
-// shared memory.  `slot` is a shared float of this CTA that every CTA of the
-// cluster reads; all CTAs add the ranks in ascending order and so agree
-// bit for bit.  Must be called by every thread of every CTA in the cluster.
-__device__ __forceinline__ float cluster_sum(float cta_value, float* slot) {
+// Split cluster barrier.  A CTA arrives (relaxed) early, e.g. at kernel start,
+// and waits just before its first access to a peer's shared memory, which is
+// then known to be live; a release-arrive / acquire-wait pair publishes
+// shared-memory stores to the peers.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Sum of one float per CTA over the thread-block cluster.  Every CTA writes
+// its value into slot[rank] of every peer (distributed shared memory), one
+// barrier publishes the stores, and each CTA adds its local slots in rank
+// order, so all CTAs agree bit for bit.  The caller has arrived on the
+// cluster barrier once (cluster_arrive_relaxed) since the kernel started;
+// every thread of every CTA in the cluster must call this.
+__device__ __forceinline__ float cluster_sum(float cta_value, float* slots) {
   cg::cluster_group cluster = cg::this_cluster();
-  if (threadIdx.x == 0) *slot = cta_value;
-  cluster.sync();
   const unsigned n = cluster.num_blocks();
+  cluster_wait_acquire();  // every peer has started: its shared memory is live
+  if (threadIdx.x < n) *cluster.map_shared_rank(slots + cluster.block_rank(), threadIdx.x) = cta_value;
+  cluster_arrive_release();
+  cluster_wait_acquire();
   float s = 0.f;
-  for (unsigned r = 0; r < n; ++r) s += *cluster.map_shared_rank(slot, r);
-  cluster.sync();  // no CTA leaves while a peer may still read its slot
+  for (unsigned r = 0; r < n; ++r) s += slots[r];
   return s;
 }
 

@@ -50,7 +50,7 @@ router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, fl
               int T, int H, int E) {
   constexpr int TILE = 16 * 8 * NT;  // outputs per tile
   __shared__ float red[WARPS][TILE];
-  __shared__ float part[TILE];
+  __shared__ float part[TILE];  // S > 1: part[src * per + i] = rank src's partial of output ib + i
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
@@ -62,6 +62,7 @@ router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, fl
   const int wb = cb + (ce - cb) * warp / WARPS;
   const int we = cb + (ce - cb) * (warp + 1) / WARPS;
 
+  if (S > 1) cluster_arrive_relaxed();
   allow_dependent_launch();
   grid_dependency_wait();
 
@@ -110,37 +111,41 @@ router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, fl
 #pragma unroll
     for (int r = 0; r < 4; ++r) red[warp][(nt * 4 + r) * 32 + lane] = acc[nt][r];
   __syncthreads();
+  if (S == 1) {
+    for (int i = tid; i < TILE; i += WARPS * 32) {
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < WARPS; ++w) s += red[w][i];
+      int e, t;
+      frag_to_tile<NT>(i, e, t);
+      if (e0 + e < E && t0 + t < T) logits[static_cast<int64_t>(t0 + t) * E + e0 + e] = s;
+    }
+    return;
+  }
+  // split-K over the cluster: rank r owns outputs [r * per, (r + 1) * per); every
+  // CTA pushes its partial of those outputs into the owner's part[], then the
+  // owner adds the S partials in rank order
+  cg::cluster_group cluster = cg::this_cluster();
+  const int me = static_cast<int>(cluster.block_rank());
+  const int per = TILE / S;  // S (a power of two <= 8) divides TILE
+  cluster_wait_acquire();  // every peer has started: its shared memory is live
   for (int i = tid; i < TILE; i += WARPS * 32) {
     float s = 0.f;
 #pragma unroll
     for (int w = 0; w < WARPS; ++w) s += red[w][i];
-    part[i] = s;
+    const int owner = i / per;
+    *cluster.map_shared_rank(part + me * per + (i - owner * per), owner) = s;
   }
-  if (S == 1) {
-    __syncthreads();
-    for (int i = tid; i < TILE; i += WARPS * 32) {
-      int e, t;
-      frag_to_tile<NT>(i, e, t);
-      if (e0 + e < E && t0 + t < T) logits[static_cast<int64_t>(t0 + t) * E + e0 + e] = part[i];
-    }
-    return;
-  }
-  cg::cluster_group cluster = cg::this_cluster();
-  cluster.sync();
-  const int per = (TILE + S - 1) / S;
-  const int ib = z * per, ie = min(TILE, ib + per);
+  cluster_arrive_release();
+  cluster_wait_acquire();
+  const int ib = me * per, ie = ib + per;
   for (int i = ib + tid; i < ie; i += WARPS * 32) {
-    float v[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r) v[r] = r < S ? cluster.map_shared_rank(part, r)[i] : 0.f;
     float s = 0.f;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) s += v[r];  // ranks in ascending order (zeros past S)
+    for (int r = 0; r < S; ++r) s += part[r * per + (i - ib)];
     int e, t;
     frag_to_tile<NT>(i, e, t);
     if (e0 + e < E && t0 + t < T) logits[static_cast<int64_t>(t0 + t) * E + e0 + e] = s;
   }
-  cluster.sync();  // keep this CTA's partial tile alive until every peer has read it
 }
 
 // Decode sizes (T <= 64): tiles of 8 or 16 tokens, 8 warps splitting each

@@ -52,7 +52,7 @@ tail_kernel(const TailParams p) {
   __shared__ int map_s[MOE_MAX_K];
   __shared__ float w_s[MOE_MAX_K];
   __shared__ float red[33];
-  __shared__ float cluster_slot;
+  __shared__ float cluster_slots[8];
 
   const int t = blockIdx.y;
   const int tid = threadIdx.x;
@@ -66,8 +66,27 @@ tail_kernel(const TailParams p) {
   const int64_t row_off = static_cast<int64_t>(t) * p.H;
   const int k = p.k;
 
+  if (cs > 1) cluster_arrive_relaxed();
   allow_dependent_launch();
   grid_dependency_wait();
+
+  int vidx[VPT];
+  bool vok[VPT];
+#pragma unroll
+  for (int m = 0; m < VPT; ++m) {
+    vidx[m] = vbeg + m * nthr + tid;
+    vok[m] = vidx[m] < vend;
+  }
+
+  // -- shared expert and residual: issued first (they do not depend on the
+  //    map), consumed last
+  uint4 sh[VPT], res[VPT];
+#pragma unroll
+  for (int m = 0; m < VPT; ++m) {
+    const int64_t off = row_off + static_cast<int64_t>(vidx[m]) * 8;
+    sh[m] = (p.shared && vok[m]) ? ld_stream16(p.shared + off) : make_uint4(0, 0, 0, 0);
+    res[m] = vok[m] ? ld_stream16(p.residual + off) : make_uint4(0, 0, 0, 0);
+  }
 
   // -- slot table: map entries (checked) and, without routing, the weights
   if (tid < k) {
@@ -80,23 +99,6 @@ tail_kernel(const TailParams p) {
     if (!ROUTE) w_s[tid] = p.topk_w[static_cast<int64_t>(t) * k + tid];
   }
   __syncthreads();
-
-  int vidx[VPT];
-  bool vok[VPT];
-#pragma unroll
-  for (int m = 0; m < VPT; ++m) {
-    vidx[m] = vbeg + m * nthr + tid;
-    vok[m] = vidx[m] < vend;
-  }
-
-  // -- shared expert and residual: issued first, consumed last
-  uint4 sh[VPT], res[VPT];
-#pragma unroll
-  for (int m = 0; m < VPT; ++m) {
-    const int64_t off = row_off + static_cast<int64_t>(vidx[m]) * 8;
-    sh[m] = (p.shared && vok[m]) ? ld_stream16(p.shared + off) : make_uint4(0, 0, 0, 0);
-    res[m] = vok[m] ? ld_stream16(p.residual + off) : make_uint4(0, 0, 0, 0);
-  }
 
   float acc[VPT][8];
 #pragma unroll
@@ -211,7 +213,7 @@ tail_kernel(const TailParams p) {
   }
 
   ss = block_sum(ss, red);
-  if (cs > 1) ss = cluster_sum(ss, &cluster_slot);
+  if (cs > 1) ss = cluster_sum(ss, cluster_slots);
   const float inv = rsqrtf(ss / static_cast<float>(p.H) + p.eps);
 
   // -- RMSNorm output

@@ -192,6 +192,9 @@ FIN = [  # name, T, H, E, k, extra kwargs
     ("stream-h8192", 320, 8192, 64, 8, dict(seed=19, s=4.0)),
     ("stream-shared-only", 304, 1024, 16, 0, dict(seed=20)),
     ("stream-padded", 350, 768, 16, 8, dict(seed=21, n_rows=4000)),
+    # T >= 8 tokens per SM: one CTA per row instead of a 2-CTA cluster
+    ("stream-single-cta", 1300, 2048, 64, 8, dict(seed=22)),
+    ("stream-single-cta-h2056", 1250, 2056, 64, 4, dict(seed=23, R=1)),
 ]
 
 
