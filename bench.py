@@ -378,11 +378,15 @@ def run_ours(args):
 
 
 def run_e2e(torch, M, layers, stream, K, warmup):
-    """Same step, host buffers: every step copies its activations (x, expert
-    rows, map, shared, residual) from one pinned host staging buffer to the
-    device in a single copy, makes the three C-ABI calls, and copies both
-    outputs back to a pinned host buffer in a single copy; timed with events.
-    Gate weights and gamma stay resident (model parameters)."""
+    """Same step with host buffers, as a serving loop would run it: every step
+    copies its activations (x, expert rows, map, shared, residual) from one
+    pinned host staging buffer to the device in a single copy, makes the three
+    C-ABI calls, and copies both outputs back to pinned host memory in a
+    single copy.  Copies in, compute and copies out run on three streams with
+    events between them (step i+1's input copy overlaps step i's compute); 8
+    device buffer sets rotate.  Gate weights and gamma stay resident (model
+    parameters).  Timed with events from the first copy in to the last copy
+    out."""
     d0 = layers[0]
     names_in = ["x", "rows", "map", "shared", "residual"]
     names_out = ["residual_out", "normed_out"]
@@ -410,42 +414,60 @@ def run_e2e(torch, M, layers, stream, K, warmup):
         hv[n].copy_(d0[n].cpu())
     host_out = torch.empty(n_out, dtype=torch.uint8).pin_memory()
     nsets = 8
-    dev_in = [torch.empty(n_in, dtype=torch.uint8, device=d0["x"].device) for _ in range(nsets)]
-    dev_out = [torch.empty(n_out, dtype=torch.uint8, device=d0["x"].device) for _ in range(nsets)]
+    dev = d0["x"].device
+    dev_in = [torch.empty(n_in, dtype=torch.uint8, device=dev) for _ in range(nsets)]
+    dev_out = [torch.empty(n_out, dtype=torch.uint8, device=dev) for _ in range(nsets)]
     dvi = [views(b, offs_in, names_in) for b in dev_in]
     dvo = [views(b, offs_out, names_out) for b in dev_out]
     h2d = sum(hv[n].numel() * hv[n].element_size() for n in names_in)
     d2h = sum(d0[n].numel() * d0[n].element_size() for n in names_out)
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(nsets)]
+    ev_done = [torch.cuda.Event() for _ in range(nsets)]
+    ev_out = [torch.cuda.Event() for _ in range(nsets)]
+    for e in ev_done + ev_out:
+        e.record(stream)
     s = stream.cuda_stream
     n_steps = max(1, min(K, 750))
 
     def one(i):
+        j = i % nsets
         d = layers[i % len(layers)]
-        a, o = dvi[i % nsets], dvo[i % nsets]
+        a, o = dvi[j], dvo[j]
+        s_in.wait_event(ev_done[j])       # the set's previous step has read its inputs
+        with torch.cuda.stream(s_in):
+            dev_in[j].copy_(host_in, non_blocking=True)
+            ev_in[j].record(s_in)
+        stream.wait_event(ev_in[j])
+        stream.wait_event(ev_out[j])      # the set's previous outputs have left the device
         with torch.cuda.stream(stream):
-            dev_in[i % nsets].copy_(host_in, non_blocking=True)
             M.moe_router_logits_fp32(a["x"], d["w_gate"], logits_out=d["logits"], stream=s)
             M.moe_topk_route(d["logits"], K_DEC, SCALE, topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
             M.moe_finalize_add_rmsnorm(a["rows"], a["map"], d["topk_w"], a["shared"], a["residual"], d["gamma"],
                                        d["eps"], residual_out=o["residual_out"], normed_out=o["normed_out"],
                                        stream=s)
-            host_out.copy_(dev_out[i % nsets], non_blocking=True)
+            ev_done[j].record(stream)
+        s_out.wait_event(ev_done[j])
+        with torch.cuda.stream(s_out):
+            host_out.copy_(dev_out[j], non_blocking=True)
+            ev_out[j].record(s_out)
 
     for i in range(max(warmup, 3)):
         one(i)
-    stream.synchronize()
+    torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(s_in)
     for i in range(n_steps):
         one(i)
-    e1.record(stream)
+    e1.record(s_out)
     e1.synchronize()
+    torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1000.0 / n_steps
     return {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n_steps,
-            "what": "one pinned host -> device copy of the step's activations, 3 C-ABI calls, "
-                    "one device -> pinned host copy of both outputs"}
+            "what": "per step: one pinned host -> device copy of the activations, 3 C-ABI calls, one device -> "
+                    "pinned host copy of both outputs; copies in / compute / copies out on three streams"}
 
 
 def run_sweep(torch, M, stream, l2, peak):
@@ -502,6 +524,19 @@ def run_sweep(torch, M, stream, l2, peak):
                                        stream=s)
         add("prefill fused tail (logits supplied)", T, H, fused, nb, sets)
         add("finalize+shared+residual+RMSNorm", T, H, fin, bytes_tail(T, H, K_DEC), sets)
+        del sets
+        torch.cuda.empty_cache()
+    # router GEMM at prefill sizes (a dense contraction near the tensor ridge)
+    for T in [512, 2048, 8192]:
+        H = H_DEC
+        nb = bytes_router(T, H, E_DEC)
+        sets = [device_layer(T, H, E_DEC, 1, seed=9500 + i, shared=False, router=True)
+                for i in range(nsets_for(nb))]
+
+        def rtr(d):
+            M.moe_router_logits_fp32(d["x"], d["w_gate"], logits_out=d["logits"], stream=s)
+        add("router GEMM (BF16 -> FP32 logits)", T, H, rtr, nb, sets)
+        out[-1]["TFLOPs"] = round(2.0 * T * E_DEC * H / (out[-1]["us"] * 1e-6) / 1e12, 1)
         del sets
         torch.cuda.empty_cache()
     # row-parallel partials: R=4 local partial buffers replace gather + shared

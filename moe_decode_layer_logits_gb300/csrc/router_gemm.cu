@@ -19,6 +19,7 @@
 //    order inside the tensor core changes.
 #include "host_util.h"
 #include "common.cuh"
+#include "router_tc.h"
 
 namespace moe {
 
@@ -193,6 +194,22 @@ extern "C" int moe_router_logits_fp32(const void* x_bf16, const void* w_gate_bf1
   const int nsm = sm_count();
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
   const uint16_t* W = static_cast<const uint16_t*>(w_gate_bf16);
+  if (router_tc_supported(T, H)) {
+    // prefill sizes: the tensor-memory kernel, in launches of up to 2^30 tokens
+    const int64_t per = static_cast<int64_t>(1) << 30;
+    for (int64_t t0 = 0; t0 < T; t0 += per) {
+      const int Tc = static_cast<int>(T - t0 < per ? T - t0 : per);
+      const cudaError_t e = launch_router_tc(x + t0 * H, W, logits_out + t0 * E, Tc, static_cast<int>(H),
+                                             static_cast<int>(E), nsm, stream);
+      if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MOE_ERR_CUDA;
+      }
+      const int st = launch_status();
+      if (st != MOE_OK) return st;
+    }
+    return MOE_OK;
+  }
   // decode sizes: 8- or 16-token tiles; more CTAs in flight beat reusing x
   // across a wider tile (measured at T = 64: 16-token tiles 5.3 us, 64-token 7.9 us)
   const int NT = T <= 8 ? 1 : (T <= 64 ? 2 : 4);

@@ -1,0 +1,306 @@
+// Router GEMM for prefill-size batches on the 5th-generation tensor cores:
+// logits[T, E] = x[T, H] . W[E, H]^T, BF16 operands, FP32 accumulation in
+// tensor memory (lmdeploy pull 4853, Summary: FP32 router logits through a
+// BF16 GEMM).  At T in the thousands the router is a dense contraction near
+// the tensor-core ridge, so it is tiled for tcgen05:
+//  - one CTA per 128-token x BN-expert tile (UMMA M = 128, N = BN);
+//  - warp 0 streams 64-wide K blocks of both operands with TMA (128-byte
+//    swizzle, out-of-range rows and columns zero-filled) into a 6-stage ring;
+//  - warp 1 allocates BN tensor-memory columns and one lane issues
+//    tcgen05.mma (kind::f16, 4 per K block), releasing each stage with
+//    tcgen05.commit when the MMAs that read it complete;
+//  - warps 2..5 wait for the final commit and read the accumulator with
+//    tcgen05.ld (each warp its 32-lane quarter = 32 tokens), storing FP32 rows.
+// Every wait is bounded; a tile whose pipeline gave up is written as NaN so
+// that the failure is visible in the output.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "host_util.h"
+#include "router_tc.h"
+
+namespace moe {
+
+constexpr int kTcBM = 128;       // tokens per tile (UMMA M)
+constexpr int kTcBK = 64;        // K elements per stage: one 128-byte swizzle row
+constexpr int kTcStages = 6;
+constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
+constexpr int kTcMaxWaits = 1 << 21;
+constexpr uint32_t kTcHintNs = 1000;
+
+template <int BN>
+struct TcSmem {
+  uint8_t a[kTcStages][kTcBM * kTcBK * 2];  // 16 KB per stage, 1024-byte aligned
+  uint8_t b[kTcStages][BN * kTcBK * 2];     // BN * 128 bytes per stage
+  uint64_t full[kTcStages];
+  uint64_t empty[kTcStages];
+  uint64_t tmem_full;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// ---- tcgen05 / TMA primitives --------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms, so the
+// stride between 8-row groups is 1024 bytes; the leading offset is not used by
+// swizzled K-major layouts.  Bits: start >> 4 [0,14), leading offset >> 4
+// [16,30), stride offset >> 4 [32,46), descriptor version 1 [46,48), swizzle
+// mode 2 = 128-byte [61,64).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16 with BF16 A and B, FP32 D, both
+// operands K-major: D format [4,6) = 1, A format [7,10) = 1, B format [10,13)
+// = 1, N >> 3 at [17,23), M >> 4 at [24,29).
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05.mma issued so far by this thread completes.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Bounded wait; gives up early once the CTA's abort flag is raised unless
+// `drain` is set (a drain must see the phase, abort or not).
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, bool drain) {
+  for (int it = 0; it < kTcMaxWaits; ++it) {
+    if (mbar_try_wait(bar, parity, kTcHintNs)) return true;
+    if (!drain && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kTcThreads, 1)
+router_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+                 float* __restrict__ logits, int T, int H, int E) {
+  extern __shared__ uint8_t smem_raw[];
+  TcSmem<BN>& sm = *reinterpret_cast<TcSmem<BN>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                  ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * kTcBM, n0 = blockIdx.y * BN;
+  const int nkb = (H + kTcBK - 1) / kTcBK;
+  volatile int* abort_v = &sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    mbar_init(&sm.tmem_full, 1);
+    sm.abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 1) tmem_alloc(&sm.tmem_base, BN);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_d = sm.tmem_base;
+
+  allow_dependent_launch();
+  grid_dependency_wait();
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % kTcStages, n = kb / kTcStages;
+        if (n > 0 && !tc_wait(&sm.empty[s], (n - 1) & 1, abort_v, false)) break;
+        mbar_arrive_expect_tx(&sm.full[s], static_cast<uint32_t>((kTcBM + BN) * kTcBK * 2));
+        tma_load_2d(sm.a[s], &tmap_x, kb * kTcBK, m0, &sm.full[s]);
+        tma_load_2d(sm.b[s], &tmap_w, kb * kTcBK, n0, &sm.full[s]);
+        issued = kb + 1;
+      }
+      // drain: no copy may land after this CTA exits
+      for (int kb = issued > kTcStages ? issued - kTcStages : 0; kb < issued; ++kb)
+        tc_wait(&sm.full[kb % kTcStages], (kb / kTcStages) & 1, abort_v, true);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_bf16(kTcBM, BN);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % kTcStages, n = kb / kTcStages;
+        if (!tc_wait(&sm.full[s], n & 1, abort_v, false)) break;
+        tc_fence_after_sync();
+        const uint32_t a0 = smem_addr(sm.a[s]), b0 = smem_addr(sm.b[s]);
+#pragma unroll
+        for (int kk = 0; kk < kTcBK / 16; ++kk) {  // 16 BF16 = 32 bytes of K per MMA
+          umma_bf16(tmem_d, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32), idesc,
+                    (kb | kk) != 0);
+        }
+        umma_commit(&sm.empty[s]);
+      }
+      umma_commit(&sm.tmem_full);  // also after an abort: it fires once issued MMAs are done
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // this warp's 32-lane quarter of tensor memory
+    const bool ok = tc_wait(&sm.tmem_full, 0, abort_v, true) && !*abort_v;
+    tc_fence_after_sync();
+    const int row = m0 + q * 32 + lane;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t v[32];
+      tmem_ld_32cols(tmem_d + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c), v);
+      if (row < T) {
+        float* dst = logits + static_cast<int64_t>(row) * E + n0 + c;
+        const int nvalid = min(32, E - (n0 + c));
+        if (nvalid == 32 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            float4 f;
+            f.x = ok ? __uint_as_float(v[i]) : __int_as_float(0x7FC00000);
+            f.y = ok ? __uint_as_float(v[i + 1]) : __int_as_float(0x7FC00000);
+            f.z = ok ? __uint_as_float(v[i + 2]) : __int_as_float(0x7FC00000);
+            f.w = ok ? __uint_as_float(v[i + 3]) : __int_as_float(0x7FC00000);
+            *reinterpret_cast<float4*>(dst + i) = f;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i < nvalid) dst[i] = ok ? __uint_as_float(v[i]) : __int_as_float(0x7FC00000);
+        }
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_d, BN);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Row-major BF16 [rows, cols] matrix, boxes of box_rows x 64 with the 128-byte swizzle.
+static bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN>
+static cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw, float* logits, int T, int H, int E,
+                             cudaStream_t stream) {
+  const size_t smem = sizeof(TcSmem<BN>) + 1024;
+  static bool opt_in[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (dev >= 0 && dev < 64 && !opt_in[dev]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(router_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    opt_in[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((T + kTcBM - 1) / kTcBM, (E + BN - 1) / BN, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, router_tc_kernel<BN>, mx, mw, logits, T, H, E);
+}
+
+cudaError_t launch_router_tc(const void* x, const void* w, float* logits, int T, int H, int E, int nsm,
+                             cudaStream_t stream) {
+  // 128 expert columns per tile when that still gives most SMs a tile, else 64
+  const int mt = (T + kTcBM - 1) / kTcBM;
+  const int bn = static_cast<int64_t>(mt) * ((E + 127) / 128) >= nsm * 3 / 4 ? 128 : 64;
+  CUtensorMap mx, mw;
+  if (!make_map(&mx, x, T, H, kTcBM) || !make_map(&mw, w, E, H, bn)) return cudaErrorInvalidValue;
+  return bn == 128 ? launch_tc<128>(mx, mw, logits, T, H, E, stream)
+                   : launch_tc<64>(mx, mw, logits, T, H, E, stream);
+}
+
+bool router_tc_supported(int64_t T, int64_t H) { return T >= kRouterTcMinT && H >= kTcBK; }
+
+}  // namespace moe

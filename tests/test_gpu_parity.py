@@ -51,6 +51,9 @@ def bits(t):
 ROUTER = [  # (T, H, E)
     (4, 2048, 64), (1, 6144, 256), (4, 6144, 256), (64, 6144, 256), (12, 6144, 256), (28, 2048, 256),
     (37, 2056, 72), (300, 6144, 256), (5, 512, 20), (3, 64, 1), (9, 1024, 1024), (16, 8, 16), (130, 6144, 168),
+    # from 1024 tokens the tcgen05 kernel: full and partial 128-token tiles, partial
+    # 64-wide K blocks (H = 2056) and partial expert tiles (E = 168, 72, 1)
+    (1024, 6144, 256), (1500, 2056, 168), (1100, 512, 72), (1024, 64, 1), (1280, 1024, 1024),
 ]
 
 
@@ -63,6 +66,19 @@ def test_router_logits(M, T, H, E):
     g = M.moe_router_logits_fp32(dev(x), dev(w)).cpu().numpy().astype(np.float64)
     err = np.abs(g - L)
     assert np.all(err <= 1e-5 * A + 1e-30), float(np.max(err / np.maximum(A, 1e-30)))
+
+
+def test_router_logits_misaligned_output(M):
+    # logits need only 4-byte alignment: write through an offset view
+    T, H, E = 1024, 512, 64
+    rng = np.random.default_rng(103)
+    x = draw_bf16(rng, (T, H), 1.0)
+    w = draw_bf16(rng, (E, H), 0.02)
+    buf = torch.empty(T * E + 1, dtype=torch.float32, device="cuda")
+    out = buf[1:].view(T, E)
+    M.moe_router_logits_fp32(dev(x), dev(w), logits_out=out)
+    L, A = O.router_logits(x, w)
+    assert np.all(np.abs(out.cpu().numpy().astype(np.float64) - L) <= 1e-5 * A)
 
 
 def test_router_prefill_size_sampled(M):
@@ -81,7 +97,7 @@ def test_router_small_integers_exact(M):
     # every product and partial sum is an integer below 2^24: exact in FP32
     rng = np.random.default_rng(102)
     from moe_decode_layer_logits_gb300.inputs import to_bf16_bits
-    for T, H, E in [(64, 2048, 256), (3, 2048, 64), (33, 1000, 40)]:
+    for T, H, E in [(64, 2048, 256), (3, 2048, 64), (33, 1000, 40), (1024, 2048, 256), (1130, 1016, 136)]:
         xi = rng.integers(-16, 17, size=(T, H))
         wi = rng.integers(-16, 17, size=(E, H))
         g = M.moe_router_logits_fp32(dev(to_bf16_bits(xi)), dev(to_bf16_bits(wi))).cpu().numpy()
