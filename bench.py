@@ -56,7 +56,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--min-timed-s", type=float, default=1.0,
                     help="repeat the K-step timed region until this much time is covered")
-    ap.add_argument("--ncu-case", choices=["decode", "prefill"], default=None,
+    ap.add_argument("--ncu-case", choices=["decode", "prefill", "router"], default=None,
                     help="run a small fixed case for an ncu capture and exit (no timing, no JSON)")
     return ap.parse_args()
 
@@ -384,9 +384,10 @@ def run_e2e(torch, M, layers, stream, K, warmup):
     C-ABI calls, and copies both outputs back to pinned host memory in a
     single copy.  Copies in, compute and copies out run on three streams with
     events between them (step i+1's input copy overlaps step i's compute); 8
-    device buffer sets rotate.  Gate weights and gamma stay resident (model
-    parameters).  Timed with events from the first copy in to the last copy
-    out."""
+    device buffer sets rotate; 8 steps are captured in one CUDA graph and the
+    graph is replayed.  Gate weights and gamma stay resident (model
+    parameters).  Timed with events around the replays, which include every
+    copy in and out."""
     d0 = layers[0]
     names_in = ["x", "rows", "map", "shared", "residual"]
     names_out = ["residual_out", "normed_out"]
@@ -422,52 +423,56 @@ def run_e2e(torch, M, layers, stream, K, warmup):
     h2d = sum(hv[n].numel() * hv[n].element_size() for n in names_in)
     d2h = sum(d0[n].numel() * d0[n].element_size() for n in names_out)
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_in = [torch.cuda.Event() for _ in range(nsets)]
-    ev_done = [torch.cuda.Event() for _ in range(nsets)]
-    ev_out = [torch.cuda.Event() for _ in range(nsets)]
-    for e in ev_done + ev_out:
-        e.record(stream)
     s = stream.cuda_stream
-    n_steps = max(1, min(K, 750))
 
-    def one(i):
-        j = i % nsets
-        d = layers[i % len(layers)]
-        a, o = dvi[j], dvo[j]
-        s_in.wait_event(ev_done[j])       # the set's previous step has read its inputs
-        with torch.cuda.stream(s_in):
-            dev_in[j].copy_(host_in, non_blocking=True)
-            ev_in[j].record(s_in)
-        stream.wait_event(ev_in[j])
-        stream.wait_event(ev_out[j])      # the set's previous outputs have left the device
-        with torch.cuda.stream(stream):
-            M.moe_router_logits_fp32(a["x"], d["w_gate"], logits_out=d["logits"], stream=s)
-            M.moe_topk_route(d["logits"], K_DEC, SCALE, topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
-            M.moe_finalize_add_rmsnorm(a["rows"], a["map"], d["topk_w"], a["shared"], a["residual"], d["gamma"],
-                                       d["eps"], residual_out=o["residual_out"], normed_out=o["normed_out"],
-                                       stream=s)
-            ev_done[j].record(stream)
-        s_out.wait_event(ev_done[j])
-        with torch.cuda.stream(s_out):
-            host_out.copy_(dev_out[j], non_blocking=True)
-            ev_out[j].record(s_out)
+    def steps(n):
+        # step j: copy in on s_in, compute on `stream`, copy out on s_out
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for j in range(n):
+            d = layers[j % len(layers)]
+            a, o = dvi[j % nsets], dvo[j % nsets]
+            with torch.cuda.stream(s_in):
+                dev_in[j % nsets].copy_(host_in, non_blocking=True)
+            stream.wait_stream(s_in)
+            with torch.cuda.stream(stream):
+                M.moe_router_logits_fp32(a["x"], d["w_gate"], logits_out=d["logits"], stream=s)
+                M.moe_topk_route(d["logits"], K_DEC, SCALE, topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
+                M.moe_finalize_add_rmsnorm(a["rows"], a["map"], d["topk_w"], a["shared"], a["residual"],
+                                           d["gamma"], d["eps"], residual_out=o["residual_out"],
+                                           normed_out=o["normed_out"], stream=s)
+            s_out.wait_stream(stream)
+            with torch.cuda.stream(s_out):
+                host_out.copy_(dev_out[j % nsets], non_blocking=True)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
 
-    for i in range(max(warmup, 3)):
-        one(i)
+    # a serving loop replays captured steps: one graph of `nsets` steps
+    with torch.cuda.stream(stream):
+        steps(nsets)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        steps(nsets)
+    reps = max(1, (min(K, 750) + nsets - 1) // nsets)
+    n_steps = reps * nsets
+    for _ in range(max(1, warmup // nsets)):
+        g.replay()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(s_in)
-    for i in range(n_steps):
-        one(i)
-    e1.record(s_out)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
     e1.synchronize()
-    torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1000.0 / n_steps
     return {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n_steps,
             "what": "per step: one pinned host -> device copy of the activations, 3 C-ABI calls, one device -> "
-                    "pinned host copy of both outputs; copies in / compute / copies out on three streams"}
+                    "pinned host copy of both outputs; copies in / compute / copies out on three streams, "
+                    "8 steps per captured graph"}
 
 
 def run_sweep(torch, M, stream, l2, peak):
@@ -624,11 +629,21 @@ def run_ncu_case(case):
     """Small cases for ncu captures (a few hundred MB, more than the L2):
     decode -- 12 layers at T=64 (162 MB), router -> route -> finalize on each
     layer, twice; prefill -- 2 sets at T=2048 (605 MB), route, finalize and the
-    router-less fused tail on each set, twice."""
+    router-less fused tail on each set, twice; router -- the router GEMM on 2
+    inputs at T=8192 (x 100 MB each), twice."""
     import torch
     import moe_decode_layer_logits_gb300 as M
     from moe_decode_layer_logits_gb300.inputs import device_layer
     M.lib()
+    if case == "router":
+        # 2 router inputs at T=8192 (x 100 MB each): the tensor-memory router kernel, twice each
+        sets = [device_layer(8192, H_DEC, E_DEC, 1, seed=200 + i, shared=False) for i in range(2)]
+        torch.cuda.synchronize()
+        for _ in range(2):
+            for d in sets:
+                M.moe_router_logits_fp32(d["x"], d["w_gate"], logits_out=d["logits"])
+        torch.cuda.synchronize()
+        return
     if case == "decode":
         sets = [device_layer(T_DEC, H_DEC, E_DEC, K_DEC, seed=i, scale=SCALE) for i in range(12)]
     else:

@@ -132,6 +132,27 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile
   return false;
 }
 
+// Store 32 consecutive FP32 values of one row (the first `nvalid`), as 16-byte
+// vectors when the row slice is aligned; NaN when the pipeline gave up.
+__device__ __forceinline__ void store_row32(float* dst, const uint32_t (&v)[32], int nvalid, bool ok) {
+  const float nan = __int_as_float(0x7FC00000);
+  if (nvalid == 32 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      float4 f;
+      f.x = ok ? __uint_as_float(v[i]) : nan;
+      f.y = ok ? __uint_as_float(v[i + 1]) : nan;
+      f.z = ok ? __uint_as_float(v[i + 2]) : nan;
+      f.w = ok ? __uint_as_float(v[i + 3]) : nan;
+      *reinterpret_cast<float4*>(dst + i) = f;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nvalid) dst[i] = ok ? __uint_as_float(v[i]) : nan;
+  }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kTcThreads, 1)
 router_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
@@ -141,7 +162,10 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
                                                   ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * kTcBM, n0 = blockIdx.y * BN;
-  const int nkb = (H + kTcBK - 1) / kTcBK;
+  const int S = gridDim.z;  // split-K: the cluster's CTAs take consecutive K ranges
+  const int nkb_all = (H + kTcBK - 1) / kTcBK;
+  const int kb0 = static_cast<int>(static_cast<int64_t>(nkb_all) * blockIdx.z / S);
+  const int nkb = static_cast<int>(static_cast<int64_t>(nkb_all) * (blockIdx.z + 1) / S) - kb0;
   volatile int* abort_v = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -170,8 +194,8 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
         const int s = kb % kTcStages, n = kb / kTcStages;
         if (n > 0 && !tc_wait(&sm.empty[s], (n - 1) & 1, abort_v, false)) break;
         mbar_arrive_expect_tx(&sm.full[s], static_cast<uint32_t>((kTcBM + BN) * kTcBK * 2));
-        tma_load_2d(sm.a[s], &tmap_x, kb * kTcBK, m0, &sm.full[s]);
-        tma_load_2d(sm.b[s], &tmap_w, kb * kTcBK, n0, &sm.full[s]);
+        tma_load_2d(sm.a[s], &tmap_x, (kb0 + kb) * kTcBK, m0, &sm.full[s]);
+        tma_load_2d(sm.b[s], &tmap_w, (kb0 + kb) * kTcBK, n0, &sm.full[s]);
         issued = kb + 1;
       }
       // drain: no copy may land after this CTA exits
@@ -197,34 +221,68 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
       umma_commit(&sm.tmem_full);  // also after an abort: it fires once issued MMAs are done
     }
     __syncwarp();
-  } else {
-    // ---------------------------------------------------------------- epilogue
-    const int q = warp & 3;  // this warp's 32-lane quarter of tensor memory
-    const bool ok = tc_wait(&sm.tmem_full, 0, abort_v, true) && !*abort_v;
+  }
+  // ------------------------------------------------------------------ epilogue
+  // Warps 2..5 own tensor-memory lane quarter q = warp % 4 (32 tokens each).
+  // Without split-K they store their rows.  With split-K every CTA of the
+  // cluster pushes its partial rows into the shared memory of the CTA that
+  // owns them (rows [r * 128/S, (r+1) * 128/S) belong to rank r; the stage
+  // ring is free by then), and each owner adds the S partials in rank order.
+  __syncwarp();  // warps 0 and 1 reconverge after their lane-0 loops
+  const bool epi = warp >= 2;
+  const int q = warp & 3;
+  const int row_t = q * 32 + lane;  // row of the tile
+  bool ok = true;
+  if (epi) {
+    ok = tc_wait(&sm.tmem_full, 0, abort_v, true) && !*abort_v;
     tc_fence_after_sync();
-    const int row = m0 + q * 32 + lane;
+  }
+  constexpr int PITCH = BN + 4;  // floats per received row (padding spreads the banks)
+  if (S == 1) {
+    if (epi) {
+      const int row = m0 + row_t;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t v[32];
-      tmem_ld_32cols(tmem_d + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c), v);
-      if (row < T) {
-        float* dst = logits + static_cast<int64_t>(row) * E + n0 + c;
-        const int nvalid = min(32, E - (n0 + c));
-        if (nvalid == 32 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t v[32];
+        tmem_ld_32cols(tmem_d + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c), v);
+        if (row < T) store_row32(logits + static_cast<int64_t>(row) * E + n0 + c, v, min(32, E - (n0 + c)), ok);
+      }
+    }
+  } else {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rpo = kTcBM / S;                 // rows owned per rank
+    float* recv = reinterpret_cast<float*>(&sm.a[0][0]);  // [S][rpo][PITCH]
+    cluster_arrive_release();                  // every CTA's MMAs are done; stage rings are free
+    cluster_wait_acquire();
+    if (epi) {
+      const int owner = row_t / rpo, rl = row_t - owner * rpo;
+      float* dst = cluster.map_shared_rank(recv, owner) +
+                   (static_cast<int>(cluster.block_rank()) * rpo + rl) * PITCH;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t v[32];
+        tmem_ld_32cols(tmem_d + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c), v);
+        const float nan = __int_as_float(0x7FC00000);
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            float4 f;
-            f.x = ok ? __uint_as_float(v[i]) : __int_as_float(0x7FC00000);
-            f.y = ok ? __uint_as_float(v[i + 1]) : __int_as_float(0x7FC00000);
-            f.z = ok ? __uint_as_float(v[i + 2]) : __int_as_float(0x7FC00000);
-            f.w = ok ? __uint_as_float(v[i + 3]) : __int_as_float(0x7FC00000);
-            *reinterpret_cast<float4*>(dst + i) = f;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (i < nvalid) dst[i] = ok ? __uint_as_float(v[i]) : __int_as_float(0x7FC00000);
-        }
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(dst + c + i) =
+              ok ? make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
+                               __uint_as_float(v[i + 3]))
+                 : make_float4(nan, nan, nan, nan);
+      }
+    }
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    if (epi) {
+      const int me = static_cast<int>(cluster.block_rank());
+      const int et = threadIdx.x - 64;  // 0..127
+      for (int e = et; e < rpo * BN; e += 128) {
+        const int rl = e / BN, col = e - rl * BN;
+        float acc = 0.f;
+        for (int r = 0; r < S; ++r) acc += recv[(r * rpo + rl) * PITCH + col];
+        const int row = m0 + me * rpo + rl;
+        if (row < T && n0 + col < E)
+          logits[static_cast<int64_t>(row) * E + n0 + col] = ok ? acc : __int_as_float(0x7FC00000);  // a peer's NaN propagates
       }
     }
   }
@@ -268,7 +326,7 @@ static bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t c
 
 template <int BN>
 static cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw, float* logits, int T, int H, int E,
-                             cudaStream_t stream) {
+                             int S, cudaStream_t stream) {
   const size_t smem = sizeof(TcSmem<BN>) + 1024;
   static bool opt_in[64] = {false};
   int dev = 0;
@@ -280,25 +338,42 @@ static cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw, float
     opt_in[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((T + kTcBM - 1) / kTcBM, (E + BN - 1) / BN, 1);
+  cfg.gridDim = dim3((T + kTcBM - 1) / kTcBM, (E + BN - 1) / BN, S);
   cfg.blockDim = dim3(kTcThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1] = {pdl_attribute()};
-  cfg.attrs = attr;
+  cudaLaunchAttribute attr[2];
+  attr[0] = pdl_attribute();
   cfg.numAttrs = 1;
+  if (S > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = S;
+    cfg.numAttrs = 2;
+  }
+  cfg.attrs = attr;
   return cudaLaunchKernelEx(&cfg, router_tc_kernel<BN>, mx, mw, logits, T, H, E);
 }
 
 cudaError_t launch_router_tc(const void* x, const void* w, float* logits, int T, int H, int E, int nsm,
                              cudaStream_t stream) {
-  // 128 expert columns per tile when that still gives most SMs a tile, else 64
+  // 128 expert columns per tile (64 for E <= 64); then split K over a cluster of
+  // S CTAs until the grid covers about three quarters of the SMs: a CTA's time
+  // is set by its K blocks, since each SM streams at its own latency-bound
+  // rate.  S = 8 only while the grid stays within 64 CTAs: sixteen clusters of
+  // 8 CTAs of ~200 KB shared memory did not all fit in one wave (T = 1024:
+  // 24 us with S = 8 against 13 us for eight such clusters at T = 512).
   const int mt = (T + kTcBM - 1) / kTcBM;
-  const int bn = static_cast<int64_t>(mt) * ((E + 127) / 128) >= nsm * 3 / 4 ? 128 : 64;
+  const int bn = E > 64 ? 128 : 64;
+  const int tiles = mt * ((E + bn - 1) / bn);
+  const int nkb = (H + kTcBK - 1) / kTcBK;
+  int S = 1;
+  while (S < 8 && tiles * S < nsm * 3 / 4 && nkb >= 2 * S * 2 && (S < 4 || tiles * 2 * S <= 64)) S *= 2;
   CUtensorMap mx, mw;
   if (!make_map(&mx, x, T, H, kTcBM) || !make_map(&mw, w, E, H, bn)) return cudaErrorInvalidValue;
-  return bn == 128 ? launch_tc<128>(mx, mw, logits, T, H, E, stream)
-                   : launch_tc<64>(mx, mw, logits, T, H, E, stream);
+  return bn == 128 ? launch_tc<128>(mx, mw, logits, T, H, E, S, stream)
+                   : launch_tc<64>(mx, mw, logits, T, H, E, S, stream);
 }
 
 bool router_tc_supported(int64_t T, int64_t H) { return T >= kRouterTcMinT && H >= kTcBK; }
