@@ -179,6 +179,21 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// Hint: bring `bytes` (a multiple of 16, 16-byte aligned) at `src` into the
+// L2.  Only a hint -- later loads still observe every write made before them
+// -- so it may be issued before grid_dependency_wait().
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Relaxed load used only to choose prefetch addresses before the dependency
+// wait (the value may be stale; it is never used for results).
+__device__ __forceinline__ int ld_relaxed_s32(const int32_t* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ uint4 lds16(const void* p) {
   return *reinterpret_cast<const uint4*>(p);
 }

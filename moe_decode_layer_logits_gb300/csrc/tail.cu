@@ -68,7 +68,29 @@ tail_kernel(const TailParams p) {
 
   if (cs > 1) cluster_arrive_relaxed();
   allow_dependent_launch();
+  // While the previous kernel finishes: L2 prefetch of this CTA's slice of the
+  // token's rows (hints only; the loads below come after the dependency wait
+  // and see the final data whatever the prefetch fetched).
+  {
+    const int64_t sb = static_cast<int64_t>(vbeg) * 8, slen = static_cast<int64_t>(vend - vbeg) * 16;
+    if (slen > 0) {
+      if (tid == 0) prefetch_l2(p.residual + row_off + sb, static_cast<uint32_t>(slen));
+      if (tid == 1 && p.shared) prefetch_l2(p.shared + row_off + sb, static_cast<uint32_t>(slen));
+      if (tid == 2) prefetch_l2(p.gamma + sb, static_cast<uint32_t>(slen * 2));
+      if (tid >= 32 && tid < 32 + k) {
+        const int m = ld_relaxed_s32(p.map + static_cast<int64_t>(t) * k + (tid - 32));
+        if (m >= 0 && static_cast<int64_t>(m) < p.n_rows)
+          prefetch_l2(p.rows + static_cast<int64_t>(m) * p.H + sb, static_cast<uint32_t>(slen));
+      }
+    }
+  }
   grid_dependency_wait();
+
+  // router-less variant: warp 0 requests the token's logits first, so the
+  // selection below overlaps the expert-row gathers
+  constexpr int KEYS = EPL > 0 ? EPL : 1;
+  uint32_t keys[KEYS];
+  if (ROUTE && tid < 32) route_load_keys<KEYS>(p.logits + static_cast<int64_t>(t) * p.E, p.E, keys);
 
   int vidx[VPT];
   bool vok[VPT];
@@ -125,7 +147,7 @@ tail_kernel(const TailParams p) {
       if (tid < 32) {
         int id;
         float w;
-        warp_route<(EPL > 0 ? EPL : 1)>(p.logits + static_cast<int64_t>(t) * p.E, p.E, k, p.scale, id, w);
+        route_select<KEYS>(keys, k, p.scale, id, w);
         if (tid < k) {
           w_s[tid] = w;
           if (rank == 0) {
