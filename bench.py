@@ -494,6 +494,7 @@ def run_sweep(torch, M, stream, l2, peak):
     for T, H in [(1, 6144), (4, 6144), (64, 6144), (12, 6144), (28, 6144), (12, 2048), (28, 2048)]:
         nb = bytes_router(T, H, E_DEC) + bytes_route(T, E_DEC, K_DEC) + bytes_tail(T, H, K_DEC)
         sets = [device_layer(T, H, E_DEC, K_DEC, seed=7000 + i, scale=SCALE) for i in range(nsets_for(nb))]
+        torch.cuda.synchronize()  # the buffers are drawn on torch's stream; the kernels run on `stream`
 
         def full(d):
             M.moe_router_logits_fp32(d["x"], d["w_gate"], logits_out=d["logits"], stream=s)
@@ -515,6 +516,7 @@ def run_sweep(torch, M, stream, l2, peak):
         nb = bytes_tail(T, H, K_DEC, E=E_DEC)
         sets = [device_layer(T, H, E_DEC, K_DEC, seed=8000 + i, scale=SCALE, router=False, logits=True)
                 for i in range(nsets_for(nb))]
+        torch.cuda.synchronize()
         for d in sets:
             M.moe_topk_route(d["logits"], K_DEC, SCALE, topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
 
@@ -537,6 +539,7 @@ def run_sweep(torch, M, stream, l2, peak):
         nb = bytes_router(T, H, E_DEC)
         sets = [device_layer(T, H, E_DEC, 1, seed=9500 + i, shared=False, router=True)
                 for i in range(nsets_for(nb))]
+        torch.cuda.synchronize()
 
         def rtr(d):
             M.moe_router_logits_fp32(d["x"], d["w_gate"], logits_out=d["logits"], stream=s)
@@ -550,6 +553,7 @@ def run_sweep(torch, M, stream, l2, peak):
         nb = bytes_tail(T, H, 0, shared=False, R=4)
         sets = [device_layer(T, H, E_DEC, 0, seed=9000 + i, shared=False, R=4, router=False)
                 for i in range(nsets_for(nb))]
+        torch.cuda.synchronize()
 
         def part(d):
             M.moe_finalize_add_rmsnorm(None, None, None, None, d["residual"], d["gamma"], d["eps"],

@@ -41,6 +41,14 @@ __device__ __forceinline__ void st16(void* p, uint4 v) {
 }
 
 // Unpack 8 BF16 values of a 16-byte vector into floats.
+// The same 8 values as FP32 pairs (element 2i in .x, 2i + 1 in .y).
+__device__ __forceinline__ void unpack8x2(const uint4& v, float2 f[4]) {
+  f[0] = make_float2(bf16lo(v.x), bf16hi(v.x));
+  f[1] = make_float2(bf16lo(v.y), bf16hi(v.y));
+  f[2] = make_float2(bf16lo(v.z), bf16hi(v.z));
+  f[3] = make_float2(bf16lo(v.w), bf16hi(v.w));
+}
+
 __device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
   f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
   f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
@@ -184,6 +192,14 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
 // -- so it may be issued before grid_dependency_wait().
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// L2 prefetch hint for the whole 16-byte blocks inside the n floats at `row`
+// (no byte outside the row is named).
+__device__ __forceinline__ void prefetch_row_l2(const float* row, int n) {
+  const uintptr_t b = (reinterpret_cast<uintptr_t>(row) + 15) & ~static_cast<uintptr_t>(15);
+  const uintptr_t e = (reinterpret_cast<uintptr_t>(row + n)) & ~static_cast<uintptr_t>(15);
+  if (e > b) prefetch_l2(reinterpret_cast<const void*>(b), static_cast<uint32_t>(e - b));
 }
 
 // Relaxed load used only to choose prefetch addresses before the dependency

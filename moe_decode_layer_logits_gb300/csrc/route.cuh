@@ -4,11 +4,19 @@
 // Details: the router folds the routed scaling factor into the weights).
 //
 // Lane l holds the logits of experts l, l + 32, ... as order-preserving
-// integer keys in registers.  Each of the k rounds scans the lane's keys
-// (the first maximum wins, i.e. the lowest expert of the lane), then two
-// warp reductions pick the largest key and, among lanes holding it, the
-// lowest expert index; the winner clears its key.  Key 0 marks a taken or
-// padding slot: every finite logit has a key >= 1.
+// integer keys in registers.  Two selection schemes give the same result:
+//  - rounds (any k): each of the k rounds scans the lane's keys (the first
+//    maximum wins, i.e. the lowest expert of the lane), then two warp
+//    reductions pick the largest key and, among lanes holding it, the lowest
+//    expert index; the winner clears its key;
+//  - a merge network (k <= 8, at most 8 keys per lane): each lane sorts its
+//    candidates, packed as (key, inverted expert index) so that one 64-bit
+//    order ranks by logit and then by lower expert, and five butterfly steps
+//    merge the lanes' sorted top-8 lists until every lane holds the warp's.
+// The rounds issue fewer instructions (better where many warps share an SM);
+// the network has the shorter dependency chain (better when one token's
+// routing is on the critical path).  Key 0 marks a taken or padding slot:
+// every finite logit has a key >= 1.
 #pragma once
 
 #include "common.cuh"
@@ -40,15 +48,84 @@ __device__ __forceinline__ void route_load_keys(const float* __restrict__ row, i
   }
 }
 
+// Compare-exchange leaving the larger value in `a`.
+__device__ __forceinline__ void cx_desc(uint64_t& a, uint64_t& b) {
+  const uint64_t hi = a > b ? a : b;
+  b = a > b ? b : a;
+  a = hi;
+}
+
+// The warp's 8 largest packed candidates, sorted descending, in every lane.
+// Lane l contributes experts l + 32 s (s < EPL <= 8).
+template <int EPL>
+__device__ __forceinline__ void route_top8(const uint32_t (&key)[EPL], uint64_t (&v)[8]) {
+  static_assert(EPL >= 1 && EPL <= 8, "the merge network holds 8 candidates per lane");
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 0; s < 8; ++s)
+    v[s] = s < EPL ? (static_cast<uint64_t>(key[s < EPL ? s : 0]) << 32) |
+                         static_cast<uint32_t>(~(lane + 32 * s))
+                   : 0ull;
+  // bitonic sort of the lane's 8 candidates, descending
+#pragma unroll
+  for (int size = 2; size <= 8; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          if ((i & size) == 0) cx_desc(v[i], v[j]);
+          else cx_desc(v[j], v[i]);
+        }
+      }
+    }
+  }
+  // merge with the partner lane's list: the top 8 of two descending lists a,
+  // b are max(a[i], b[7 - i]) (a bitonic sequence), sorted by three steps
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    uint64_t m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, v[7 - i], d);
+      m[i] = v[i] > o ? v[i] : o;
+    }
+#pragma unroll
+    for (int stride = 4; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if ((i & stride) == 0) cx_desc(m[i], m[i + stride]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = m[i];
+  }
+}
+
 // Select the top k (1 <= k <= min(E, 32)) of the keys held by the warp and
 // weight them.  All 32 lanes call this; lane j < k receives the j-th
-// selected expert in `id` and its weight in `w`.  Consumes `key`.
-template <int EPL>
+// selected expert in `id` and its weight in `w`.  Consumes `key`.  NETWORK
+// picks the merge network where it applies (k <= 8, EPL <= 8).
+template <int EPL, bool NETWORK>
 __device__ __forceinline__ void route_select(uint32_t (&key)[EPL], int k, float scale, int& id, float& w) {
   const int lane = threadIdx.x & 31;
   uint32_t my_key = 0u;
   int my_id = 0;
-  for (int round = 0; round < k; ++round) {
+  int rounds = k;
+  if constexpr (NETWORK && EPL <= 8) {
+    if (k <= 8) {
+      uint64_t v[8];
+      route_top8<EPL>(key, v);
+      uint64_t mine = 0ull;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i == lane) mine = v[i];
+      my_key = static_cast<uint32_t>(mine >> 32);
+      my_id = static_cast<int>(~static_cast<uint32_t>(mine));
+      rounds = 0;
+    }
+  }
+  for (int round = 0; round < rounds; ++round) {
     uint32_t bk = 0u;
     int bs = 0;
 #pragma unroll
@@ -77,12 +154,12 @@ __device__ __forceinline__ void route_select(uint32_t (&key)[EPL], int k, float 
 }
 
 // Both phases for one token row.
-template <int EPL>
+template <int EPL, bool NETWORK>
 __device__ __forceinline__ void warp_route(const float* __restrict__ row, int E, int k, float scale,
                                            int& id, float& w) {
   uint32_t key[EPL];
   route_load_keys<EPL>(row, E, key);
-  route_select<EPL>(key, k, scale, id, w);
+  route_select<EPL, NETWORK>(key, k, scale, id, w);
 }
 
 }  // namespace moe

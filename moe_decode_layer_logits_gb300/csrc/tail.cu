@@ -147,7 +147,7 @@ tail_kernel(const TailParams p) {
       if (tid < 32) {
         int id;
         float w;
-        route_select<KEYS>(keys, k, p.scale, id, w);
+        route_select<KEYS, true>(keys, k, p.scale, id, w);  // on the token's critical path
         if (tid < k) {
           w_s[tid] = w;
           if (rank == 0) {
@@ -274,10 +274,12 @@ tail_kernel(const TailParams p) {
 // drains the copies it has in flight.
 // ---------------------------------------------------------------------------
 
-constexpr int kStreamConsumerWarps = 8;
+constexpr int kStreamConsumerWarps = 12;
 constexpr int kStreamConsumers = 32 * kStreamConsumerWarps;
 constexpr int kStreamThreads = 64 + kStreamConsumers;
 constexpr int kStreamMaxStages = 8;
+constexpr int kMaxAhead = 4;  // tokens whose rows the producer requests into the L2 ahead of their copies
+constexpr int kLogitsAhead = 3;  // router-less tail: logits rows requested into the L2 this many tokens ahead
 constexpr int kWRing = 4;
 constexpr int kStreamSmemBudget = 200 * 1024;
 constexpr uint32_t kProbeHintNs = 1000;
@@ -289,6 +291,7 @@ struct StreamShape {
   int nstages;      // stages in the ring
   int rows;         // row pieces per stage: k slots, shared, R partials, residual
   int stage_bytes;  // rows * chunk * 2 rounded up to 128
+  int ahead;        // 0..kMaxAhead: tokens prefetched into the L2 ahead of the one being copied
 };
 
 __device__ __forceinline__ bool stream_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -310,6 +313,28 @@ __device__ __forceinline__ int stream_map_entry(const TailParams& p, int64_t t, 
     m = -1;
   }
   return m;
+}
+
+// Source row of piece l of token t's stage: slots 0..k-1 (expert rows through
+// the map; an unusable slot reads the residual row instead and has weight 0),
+// then shared, the R partials and the residual.
+__device__ __forceinline__ const uint16_t* stream_piece(const TailParams& p, int64_t t, int l, int rows, int slot_row) {
+  const int64_t roff = t * p.H;
+  if (l < p.k) return slot_row >= 0 ? p.rows + static_cast<int64_t>(slot_row) * p.H : p.residual + roff;
+  if (p.shared && l == p.k) return p.shared + roff;
+  if (l < rows - 1) {
+    const int r = l - p.k - (p.shared ? 1 : 0);
+    return p.partials + static_cast<int64_t>(r) * p.partial_stride + roff;
+  }
+  return p.residual + roff;
+}
+
+// L2 prefetch hints for every row piece of token t (lane l < k names slot l's
+// row).  Hints only: they change no result.
+__device__ __forceinline__ void stream_prefetch_token(const TailParams& p, int64_t t, int rows, int slot_row) {
+  const int lane = threadIdx.x & 31;
+  for (int l = lane; l < rows; l += 32)
+    prefetch_l2(stream_piece(p, t, l, rows, slot_row), static_cast<uint32_t>(p.H) * 2u);
 }
 
 template <int VPT, int EPL>
@@ -346,17 +371,40 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
   }
   __syncthreads();
   allow_dependent_launch();
+  if (warp == 0) {
+    // While the previous kernel finishes: L2 prefetch of this CTA's first
+    // tokens, their expert rows named by a relaxed read of the map.  Hints
+    // only -- every copy below comes after the dependency wait and sees the
+    // final data -- so a stale entry only wastes the hint.
+    for (int q = 0; q <= sh.ahead && q < ntok; ++q) {
+      const int64_t tq = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(q) * G;
+      int m = -1;
+      if (lane < k) {
+        m = ld_relaxed_s32(p.map + tq * k + lane);
+        if (m < 0 || static_cast<int64_t>(m) >= p.n_rows) m = -1;
+      }
+      stream_prefetch_token(p, tq, sh.rows, m);
+    }
+  } else if (tid == 32) {
+    prefetch_l2(p.gamma, static_cast<uint32_t>(H) * 4u);
+  }
   grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t pol = l2_evict_first_policy();
-    int row_cur = -1, row_nxt = -1;
-    if (ntok > 0 && lane < k) row_cur = stream_map_entry(p, blockIdx.x, lane);
+    const int ahead = sh.ahead;
+    // mrow[q]: this lane's map entry of token i + q (q <= ahead)
+    int mrow[kMaxAhead + 1];
+#pragma unroll
+    for (int q = 0; q <= kMaxAhead; ++q)
+      mrow[q] = (q <= ahead && q < ntok && lane < k)
+                    ? stream_map_entry(p, static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(q) * G, lane)
+                    : -1;
     int issued = 0;
     for (int i = 0; i < ntok && !*abort_v; ++i) {
       const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(i) * G;
-      const int64_t roff = t * H;
+      const int row_cur = mrow[0];
       for (int c = 0; c < sh.nchunks; ++c) {
         const int u = i * sh.nchunks + c, s = u % sh.nstages, n = u / sh.nstages;
         if (n > 0 && !stream_wait(&empty_bar[s], (n - 1) & 1, abort_v, p.err_flag)) break;
@@ -365,26 +413,29 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
         if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(sh.rows * clen * 2));
         __syncwarp();
         unsigned char* st = stage_mem + static_cast<size_t>(s) * sh.stage_bytes;
-        for (int l = lane; l < sh.rows; l += 32) {
-          const uint16_t* src;
-          if (l < k) {
-            // an unusable slot reads the residual row instead; its weight is 0
-            src = row_cur >= 0 ? p.rows + static_cast<int64_t>(row_cur) * H : p.residual + roff;
-          } else if (p.shared && l == k) {
-            src = p.shared + roff;
-          } else if (l < sh.rows - 1) {
-            const int r = l - k - (p.shared ? 1 : 0);
-            src = p.partials + static_cast<int64_t>(r) * p.partial_stride + roff;
-          } else {
-            src = p.residual + roff;
-          }
-          bulk_copy_g2s(st + static_cast<size_t>(l) * sh.chunk * 2, src + c0, static_cast<uint32_t>(clen * 2),
-                        &full_bar[s], pol);
-        }
+        for (int l = lane; l < sh.rows; l += 32)
+          bulk_copy_g2s(st + static_cast<size_t>(l) * sh.chunk * 2, stream_piece(p, t, l, sh.rows, row_cur) + c0,
+                        static_cast<uint32_t>(clen * 2), &full_bar[s], pol);
         issued = u + 1;
-        if (c == 0 && i + 1 < ntok && lane < k) row_nxt = stream_map_entry(p, t + G, lane);
+        if (c == 0) {
+          // the L2 prefetch window: tokens i+1..i+ahead are requested once
+          // each (all of them after the first token's first stage)
+#pragma unroll
+          for (int q = 1; q <= kMaxAhead; ++q) {
+            if (q <= ahead && i + q < ntok && (i == 0 || q == ahead))
+              stream_prefetch_token(p, t + static_cast<int64_t>(q) * G, sh.rows, mrow[q]);
+          }
+          // shift the map ring and request token i+ahead+1's entries
+#pragma unroll
+          for (int q = 0; q < kMaxAhead; ++q) mrow[q] = mrow[q + 1];
+          const int nq = i + ahead + 1;
+#pragma unroll
+          for (int q = 0; q <= kMaxAhead; ++q) {
+            if (q == ahead)
+              mrow[q] = (nq < ntok && lane < k) ? stream_map_entry(p, t + static_cast<int64_t>(ahead + 1) * G, lane) : -1;
+          }
+        }
       }
-      row_cur = row_nxt;
     }
     // drain: no copy may land after this CTA exits
     if (lane == 0) {
@@ -415,9 +466,11 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
         for (int e = 0; e < KEYS; ++e) keys_nxt[e] = keys[e];
       }
       if (i + 1 < ntok) fetch(t + G, keys, w_nxt, ok_nxt);  // next token's loads in flight
+      if (ROUTE && lane == 0 && i + kLogitsAhead < ntok)
+        prefetch_row_l2(p.logits + (t + static_cast<int64_t>(kLogitsAhead) * G) * p.E, p.E);
       if (ROUTE) {
         int id;
-        route_select<KEYS>(keys_nxt, k, p.scale, id, w);
+        route_select<KEYS, false>(keys_nxt, k, p.scale, id, w);  // runs ahead of the consumers
         if (lane < k) {
           if (p.ids_out) p.ids_out[t * k + lane] = id;
           if (p.w_out) p.w_out[t * k + lane] = w;
@@ -451,38 +504,44 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
           const int v = ct + m * kStreamConsumers;
           if (v < vb || v >= ve) continue;
           const int off = (v - vb) * 16;
-          float acc[8];
+          // element pairs in packed FP32 operations: each lane of a pair is
+          // one IEEE fma / add, in the same order as the scalar sum
+          float2 acc[4];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+          for (int e = 0; e < 4; ++e) acc[e] = make_float2(0.f, 0.f);
 #pragma unroll 4
           for (int j = 0; j < k; ++j) {
             const float w = w_ring[slot][j];
-            float f[8];
-            unpack8(lds16(st + j * pitch + off), f);
+            const float2 w2 = make_float2(w, w);
+            float2 f[4];
+            unpack8x2(lds16(st + j * pitch + off), f);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, f[e], acc[e]);
+            for (int e = 0; e < 4; ++e) acc[e] = __ffma2_rn(w2, f[e], acc[e]);
           }
           int l = k;
           if (p.shared) {
-            float f[8];
-            unpack8(lds16(st + l * pitch + off), f);
+            float2 f[4];
+            unpack8x2(lds16(st + l * pitch + off), f);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] += f[e];
+            for (int e = 0; e < 4; ++e) acc[e] = __fadd2_rn(acc[e], f[e]);
             ++l;
           }
           for (int r = 0; r < p.R; ++r, ++l) {
-            float f[8];
-            unpack8(lds16(st + l * pitch + off), f);
+            float2 f[4];
+            unpack8x2(lds16(st + l * pitch + off), f);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] += f[e];
+            for (int e = 0; e < 4; ++e) acc[e] = __fadd2_rn(acc[e], f[e]);
           }
-          float f[8];
-          unpack8(lds16(st + (sh.rows - 1) * pitch + off), f);
+          float2 f[4];
+          unpack8x2(lds16(st + (sh.rows - 1) * pitch + off), f);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            rr[m][e] = f[e] + acc[e];
-            ss = fmaf(rr[m][e], rr[m][e], ss);
+          for (int e = 0; e < 4; ++e) {
+            const float2 r2 = __fadd2_rn(f[e], acc[e]);
+            rr[m][2 * e] = r2.x;
+            rr[m][2 * e + 1] = r2.y;
           }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ss = fmaf(rr[m][e], rr[m][e], ss);
           uint4 o;
           o.x = pack_bf16x2(rr[m][0], rr[m][1]);
           o.y = pack_bf16x2(rr[m][2], rr[m][3]);
@@ -591,6 +650,7 @@ static bool stream_shape(int H, int rows, StreamShape& sh) {
       sh.nstages = ns < kStreamMaxStages ? ns : kStreamMaxStages;
       sh.rows = rows;
       sh.stage_bytes = stage;
+      sh.ahead = 1;
       return true;
     }
   }
@@ -660,6 +720,10 @@ static int launch_tail(TailParams p, int64_t T, cudaStream_t stream) {
     cudaError_t e;
     if (stream_path) {
       const int grid = Tc < nsm ? Tc : nsm;
+      // one token of rows prefetched ahead helps the finalize; the routing
+      // warp of the router-less tail is latency-bound on its logits loads,
+      // which the extra prefetch traffic slows, so it runs without
+      sh.ahead = ROUTE ? 0 : 1;
       const int vpt = (p.H / 8 + kStreamConsumers - 1) / kStreamConsumers;
       if (!ROUTE) e = launch_stream_e<0>(q, Tc, sh, grid, vpt, stream);
       else if (p.E <= 256) e = launch_stream_e<8>(q, Tc, sh, grid, vpt, stream);
