@@ -315,6 +315,20 @@ __device__ __forceinline__ int stream_map_entry(const TailParams& p, int64_t t, 
   return m;
 }
 
+// A map entry if it names a row, else -1.
+__device__ __forceinline__ int in_rows(int m, int64_t n_rows) {
+  return (m >= 0 && static_cast<int64_t>(m) < n_rows) ? m : -1;
+}
+
+// A map entry checked for use: -1 (and the error flag raised) if it names no row.
+__device__ __forceinline__ int checked_entry(const TailParams& p, int m) {
+  if (m < 0 || static_cast<int64_t>(m) >= p.n_rows) {
+    if (p.err_flag) atomicOr(p.err_flag, MOE_FLAG_BAD_INDEX);
+    return -1;
+  }
+  return m;
+}
+
 // Source row of piece l of token t's stage: slots 0..k-1 (expert rows through
 // the map; an unusable slot reads the residual row instead and has weight 0),
 // then shared, the R partials and the residual.
@@ -376,17 +390,24 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
     // tokens, their expert rows named by a relaxed read of the map.  Hints
     // only -- every copy below comes after the dependency wait and sees the
     // final data -- so a stale entry only wastes the hint.
-    for (int q = 0; q <= sh.ahead && q < ntok; ++q) {
-      const int64_t tq = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(q) * G;
-      int m = -1;
-      if (lane < k) {
-        m = ld_relaxed_s32(p.map + tq * k + lane);
-        if (m < 0 || static_cast<int64_t>(m) >= p.n_rows) m = -1;
-      }
-      stream_prefetch_token(p, tq, sh.rows, m);
+    int pm[kMaxAhead + 1];
+#pragma unroll
+    for (int q = 0; q <= kMaxAhead; ++q)  // all loads first, then the hints
+      pm[q] = (q <= sh.ahead && q < ntok && lane < k)
+                  ? ld_relaxed_s32(p.map + (static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(q) * G) * k + lane)
+                  : -1;
+#pragma unroll
+    for (int q = 0; q <= kMaxAhead; ++q) {
+      if (q <= sh.ahead && q < ntok)
+        stream_prefetch_token(p, static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(q) * G, sh.rows,
+                              in_rows(pm[q], p.n_rows));
     }
-  } else if (tid == 32) {
-    prefetch_l2(p.gamma, static_cast<uint32_t>(H) * 4u);
+  } else if (warp == 1) {
+    if (lane == 0) prefetch_l2(p.gamma, static_cast<uint32_t>(H) * 4u);
+    // router-less tail: the logits rows of the first tokens, which the
+    // routing of the first token waits for
+    if (ROUTE && lane >= 1 && lane <= kLogitsAhead && lane - 1 < ntok)
+      prefetch_row_l2(p.logits + (static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(lane - 1) * G) * p.E, p.E);
   }
   grid_dependency_wait();
 
@@ -394,17 +415,19 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
     // ------------------------------------------------------------ producer
     const uint64_t pol = l2_evict_first_policy();
     const int ahead = sh.ahead;
-    // mrow[q]: this lane's map entry of token i + q (q <= ahead)
+    // mrow[q]: this lane's raw map entry of token i + q (q <= ahead), loaded
+    // a token before it is needed and checked only where it is used, so the
+    // producer never waits on a map load it issued itself
     int mrow[kMaxAhead + 1];
 #pragma unroll
     for (int q = 0; q <= kMaxAhead; ++q)
       mrow[q] = (q <= ahead && q < ntok && lane < k)
-                    ? stream_map_entry(p, static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(q) * G, lane)
+                    ? p.map[(static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(q) * G) * k + lane]
                     : -1;
     int issued = 0;
     for (int i = 0; i < ntok && !*abort_v; ++i) {
       const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(i) * G;
-      const int row_cur = mrow[0];
+      int row_cur = -1;
       for (int c = 0; c < sh.nchunks; ++c) {
         const int u = i * sh.nchunks + c, s = u % sh.nstages, n = u / sh.nstages;
         if (n > 0 && !stream_wait(&empty_bar[s], (n - 1) & 1, abort_v, p.err_flag)) break;
@@ -413,9 +436,16 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
         if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(sh.rows * clen * 2));
         __syncwarp();
         unsigned char* st = stage_mem + static_cast<size_t>(s) * sh.stage_bytes;
-        for (int l = lane; l < sh.rows; l += 32)
-          bulk_copy_g2s(st + static_cast<size_t>(l) * sh.chunk * 2, stream_piece(p, t, l, sh.rows, row_cur) + c0,
+        // the pieces that do not depend on the map go first: they fly while
+        // the token's first map entries may still be loading
+        for (int l = k + lane; l < sh.rows; l += 32)
+          bulk_copy_g2s(st + static_cast<size_t>(l) * sh.chunk * 2, stream_piece(p, t, l, sh.rows, -1) + c0,
                         static_cast<uint32_t>(clen * 2), &full_bar[s], pol);
+        if (c == 0 && lane < k) row_cur = checked_entry(p, mrow[0]);
+        if (lane < k)
+          bulk_copy_g2s(st + static_cast<size_t>(lane) * sh.chunk * 2,
+                        stream_piece(p, t, lane, sh.rows, row_cur) + c0, static_cast<uint32_t>(clen * 2),
+                        &full_bar[s], pol);
         issued = u + 1;
         if (c == 0) {
           // the L2 prefetch window: tokens i+1..i+ahead are requested once
@@ -423,7 +453,7 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
 #pragma unroll
           for (int q = 1; q <= kMaxAhead; ++q) {
             if (q <= ahead && i + q < ntok && (i == 0 || q == ahead))
-              stream_prefetch_token(p, t + static_cast<int64_t>(q) * G, sh.rows, mrow[q]);
+              stream_prefetch_token(p, t + static_cast<int64_t>(q) * G, sh.rows, in_rows(mrow[q], p.n_rows));
           }
           // shift the map ring and request token i+ahead+1's entries
 #pragma unroll
@@ -432,7 +462,7 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
 #pragma unroll
           for (int q = 0; q <= kMaxAhead; ++q) {
             if (q == ahead)
-              mrow[q] = (nq < ntok && lane < k) ? stream_map_entry(p, t + static_cast<int64_t>(ahead + 1) * G, lane) : -1;
+              mrow[q] = (nq < ntok && lane < k) ? p.map[(t + static_cast<int64_t>(ahead + 1) * G) * k + lane] : -1;
           }
         }
       }
@@ -470,7 +500,11 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
         prefetch_row_l2(p.logits + (t + static_cast<int64_t>(kLogitsAhead) * G) * p.E, p.E);
       if (ROUTE) {
         int id;
-        route_select<KEYS, false>(keys_nxt, k, p.scale, id, w);  // runs ahead of the consumers
+        // the first token is on every consumer's critical path (the shorter
+        // dependency chain of the merge network); later ones run ahead of the
+        // consumers (the fewer instructions of the rounds)
+        if (i == 0) route_select<KEYS, true>(keys_nxt, k, p.scale, id, w);
+        else route_select<KEYS, false>(keys_nxt, k, p.scale, id, w);
         if (lane < k) {
           if (p.ids_out) p.ids_out[t * k + lane] = id;
           if (p.w_out) p.w_out[t * k + lane] = w;
@@ -720,10 +754,8 @@ static int launch_tail(TailParams p, int64_t T, cudaStream_t stream) {
     cudaError_t e;
     if (stream_path) {
       const int grid = Tc < nsm ? Tc : nsm;
-      // one token of rows prefetched ahead helps the finalize; the routing
-      // warp of the router-less tail is latency-bound on its logits loads,
-      // which the extra prefetch traffic slows, so it runs without
-      sh.ahead = ROUTE ? 0 : 1;
+      // one token of rows requested into the L2 ahead of its copies
+      sh.ahead = 1;
       const int vpt = (p.H / 8 + kStreamConsumers - 1) / kStreamConsumers;
       if (!ROUTE) e = launch_stream_e<0>(q, Tc, sh, grid, vpt, stream);
       else if (p.E <= 256) e = launch_stream_e<8>(q, Tc, sh, grid, vpt, stream);

@@ -210,9 +210,14 @@ FIN = [  # name, T, H, E, k, extra kwargs
     ("stream-h8192", 320, 8192, 64, 8, dict(seed=19, s=4.0)),
     ("stream-shared-only", 304, 1024, 16, 0, dict(seed=20)),
     ("stream-padded", 350, 768, 16, 8, dict(seed=21, n_rows=4000)),
-    # T >= 8 tokens per SM: one CTA per row instead of a 2-CTA cluster
-    ("stream-single-cta", 1300, 2048, 64, 8, dict(seed=22)),
-    ("stream-single-cta-h2056", 1250, 2056, 64, 4, dict(seed=23, R=1)),
+    # rows that fit one chunk: the remainder tokens run whole even when few
+    ("stream-one-chunk", 1300, 2048, 64, 8, dict(seed=22)),
+    ("stream-one-chunk-h2056", 1250, 2056, 64, 4, dict(seed=23, R=1)),
+    # on a 152-SM GPU: a last partial round of half the SMs, one of more than
+    # half, and 3-chunk rows with partial buffers and a short last round
+    ("stream-half-round", 380, 6144, 256, 8, dict(seed=24)),
+    ("stream-rem-over-half", 400, 6144, 64, 8, dict(seed=25, shared=False)),
+    ("stream-3-chunks", 330, 8192, 64, 4, dict(seed=26, R=3)),
 ]
 
 
