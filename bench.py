@@ -2,13 +2,15 @@
 """Benchmark of the decode MoE-layer tail on GB300 (one JSON line on stdout).
 
 Headline workload: the decode tail of one MoE layer at T=64 tokens, H=6144,
-E=256 routed experts, top-8, one shared expert -- router GEMM (BF16 x BF16 ->
-FP32 logits), top-k routing (softmax over the top-8 x 2.5), then the fused
-finalize + shared add + residual add + RMSNorm.  One step is one layer; the
-steps walk through 75 distinct layers' buffers (gate weights, activations,
-expert rows: about 1 GB, several times the L2), so every step reads cold HBM.
-Steps are replayed from a CUDA graph and timed with CUDA events on the
-launching stream.  The metric is microseconds per layer (lower is better).
+E=256 routed experts, top-8, one shared expert -- the router GEMM (BF16 x BF16
+-> FP32 logits), then the fused tail: top-k routing (softmax over the top-8 x
+2.5, ids and weights written out), finalize + shared add + residual add +
+RMSNorm, in one launch.  One step is one layer; the steps walk through 75
+distinct layers' buffers (gate weights, activations, expert rows: about 1 GB,
+several times the L2), so every step reads cold HBM.  Steps are replayed from
+a CUDA graph and timed with CUDA events on the launching stream.  The metric
+is microseconds per layer (lower is better).  The same layer through the
+three separate entry points (router, top-k, finalize) is reported beside it.
 
 Extra keys: ``roofline`` (the dominant kernel's algorithmic GB/s against the
 measured HBM copy peak), ``e2e`` (the same step with pinned-host inputs copied
@@ -42,8 +44,8 @@ METRIC = "µs/layer and HBM GB/s (% of GB300 peak) for fused MoE tail, T=1..8192
 UNIT = "µs/layer"
 T_DEC, H_DEC, E_DEC, K_DEC, SCALE = 64, 6144, 256, 8, 2.5
 N_LAYERS = 75  # distinct layer buffer sets the steps rotate through
-WORKLOAD = ("decode tail T=64 H=6144 E=256 k=8 +1 shared expert: router GEMM -> top-k route -> "
-            "finalize+shared+residual+RMSNorm")
+WORKLOAD = ("decode tail T=64 H=6144 E=256 k=8 +1 shared expert: router GEMM -> fused tail (top-k route "
+            "with ids and weights out, finalize+shared+residual+RMSNorm)")
 
 
 def parse_args():
@@ -275,7 +277,17 @@ def run_ours(args):
         M.moe_finalize_add_rmsnorm(d["rows"], d["map"], d["topk_w"], d["shared"], d["residual"], d["gamma"],
                                    d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"], stream=s)
 
+    def fused_tail(d):
+        M.moe_tail_fused(d["logits"], K_DEC, SCALE, d["rows"], d["map"], d["shared"], d["residual"], d["gamma"],
+                         d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"],
+                         topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
+
     def step(i):
+        d = layers[i % N_LAYERS]
+        router(d)
+        fused_tail(d)
+
+    def chain3_step(i):
         d = layers[i % N_LAYERS]
         router(d)
         route(d)
@@ -314,26 +326,21 @@ def run_ours(args):
 
     # -- per-kernel device time (each kernel alone, same cold rotation)
     kern = {}
-    kern["finalize"] = graph_time_per_unit(torch, lambda i: finalize(layers[i]), N_LAYERS, stream)
+    kern["fused_tail"] = graph_time_per_unit(torch, lambda i: fused_tail(layers[i]), N_LAYERS, stream)
     kern["router"] = graph_time_per_unit(torch, lambda i: router(layers[i]), N_LAYERS, stream)
     kern["route"] = graph_time_per_unit(torch, lambda i: route(layers[i]), N_LAYERS, stream)
-    b = {"finalize": bytes_tail(T_DEC, H_DEC, K_DEC), "router": bytes_router(T_DEC, H_DEC, E_DEC),
-         "route": bytes_route(T_DEC, E_DEC, K_DEC)}
-    dom = max(kern, key=lambda n: kern[n][0])
+    kern["finalize"] = graph_time_per_unit(torch, lambda i: finalize(layers[i]), N_LAYERS, stream)
+    b = {"fused_tail": bytes_tail(T_DEC, H_DEC, K_DEC, E=E_DEC, route_out=True),
+         "router": bytes_router(T_DEC, H_DEC, E_DEC), "route": bytes_route(T_DEC, E_DEC, K_DEC),
+         "finalize": bytes_tail(T_DEC, H_DEC, K_DEC)}
+    dom = max(("fused_tail", "router"), key=lambda n: kern[n][0])  # the headline step's two kernels
     dom_us = kern[dom][0]
     achieved = b[dom] / (dom_us * 1e-6) / 1e9
-    tag = {"finalize": "tail_kernel_decode_T64", "router": "router_kernel_decode_T64",
-           "route": "topk_route_kernel_decode_T64"}[dom]
+    tag = {"fused_tail": "tail_kernel_fused_decode_T64", "router": "router_kernel_decode_T64"}[dom]
     traffic = ncu_traffic(tag, T_DEC)
 
-    # -- fused variant: router + router-less fused tail
-    def fused_step(i):
-        d = layers[i]
-        router(d)
-        M.moe_tail_fused(d["logits"], K_DEC, SCALE, d["rows"], d["map"], d["shared"], d["residual"], d["gamma"],
-                         d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"],
-                         topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
-    fused_us = graph_time_per_unit(torch, fused_step, N_LAYERS, stream)
+    # -- the same layer through the three separate entry points
+    chain3_us = graph_time_per_unit(torch, chain3_step, N_LAYERS, stream)
 
     # -- end to end through the C ABI with pinned host buffers
     e2e = run_e2e(torch, M, layers, stream, K, args.warmup)
@@ -355,7 +362,7 @@ def run_ours(args):
                    "l2": f"cold: {N_LAYERS} layer buffer sets, {N_LAYERS * 13.5:.0f} MB > L2 {l2 / 2**20:.0f} MB",
                    "timing": "CUDA-graph replay, CUDA events on the launching stream",
                    "parallelism": f"replicas x{world}"},
-        "repeats": len(times), "gpu_launches": 3 * K,
+        "repeats": len(times), "gpu_launches": 2 * K,
         "clocks": clocks,
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} (hbm_gbs)", "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -363,9 +370,9 @@ def run_ours(args):
                      "traffic": None if traffic is None else round(traffic)},
         "kernels_us": {n: {"median": round(v[0], 3), "p20": round(v[1], 3), "p80": round(v[2], 3),
                            "GBps": round(b[n] / (v[0] * 1e-6) / 1e9, 1)} for n, v in kern.items()},
-        "fused_variant_us_per_layer": {"median": round(fused_us[0], 3), "p20": round(fused_us[1], 3),
-                                       "p80": round(fused_us[2], 3),
-                                       "what": "router GEMM -> router-less fused tail (2 launches)"},
+        "three_launch_chain_us_per_layer": {"median": round(chain3_us[0], 3), "p20": round(chain3_us[1], 3),
+                                            "p80": round(chain3_us[2], 3),
+                                            "what": "router GEMM -> top-k route -> finalize (3 launches)"},
         "e2e": e2e,
         "cpu_baseline": cpu,
         "sweep": sweep,
@@ -380,8 +387,8 @@ def run_ours(args):
 def run_e2e(torch, M, layers, stream, K, warmup):
     """Same step with host buffers, as a serving loop would run it: every step
     copies its activations (x, expert rows, map, shared, residual) from one
-    pinned host staging buffer to the device in a single copy, makes the three
-    C-ABI calls, and copies both outputs back to pinned host memory in a
+    pinned host staging buffer to the device in a single copy, makes the two
+    C-ABI calls (router, fused tail), and copies both outputs back to pinned host memory in a
     single copy.  Copies in, compute and copies out run on three streams with
     events between them (step i+1's input copy overlaps step i's compute); 8
     device buffer sets rotate; 8 steps are captured in one CUDA graph and the
@@ -437,10 +444,9 @@ def run_e2e(torch, M, layers, stream, K, warmup):
             stream.wait_stream(s_in)
             with torch.cuda.stream(stream):
                 M.moe_router_logits_fp32(a["x"], d["w_gate"], logits_out=d["logits"], stream=s)
-                M.moe_topk_route(d["logits"], K_DEC, SCALE, topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
-                M.moe_finalize_add_rmsnorm(a["rows"], a["map"], d["topk_w"], a["shared"], a["residual"],
-                                           d["gamma"], d["eps"], residual_out=o["residual_out"],
-                                           normed_out=o["normed_out"], stream=s)
+                M.moe_tail_fused(d["logits"], K_DEC, SCALE, a["rows"], a["map"], a["shared"], a["residual"],
+                                 d["gamma"], d["eps"], residual_out=o["residual_out"], normed_out=o["normed_out"],
+                                 topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
             s_out.wait_stream(stream)
             with torch.cuda.stream(s_out):
                 host_out.copy_(dev_out[j % nsets], non_blocking=True)
@@ -470,7 +476,7 @@ def run_e2e(torch, M, layers, stream, K, warmup):
     us = e0.elapsed_time(e1) * 1000.0 / n_steps
     return {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n_steps,
-            "what": "per step: one pinned host -> device copy of the activations, 3 C-ABI calls, one device -> "
+            "what": "per step: one pinned host -> device copy of the activations, 2 C-ABI calls, one device -> "
                     "pinned host copy of both outputs; copies in / compute / copies out on three streams, "
                     "8 steps per captured graph"}
 
@@ -507,6 +513,14 @@ def run_sweep(torch, M, stream, l2, peak):
             M.moe_finalize_add_rmsnorm(d["rows"], d["map"], d["topk_w"], d["shared"], d["residual"], d["gamma"],
                                        d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"],
                                        stream=s)
+
+        def fusedl(d):
+            M.moe_router_logits_fp32(d["x"], d["w_gate"], logits_out=d["logits"], stream=s)
+            M.moe_tail_fused(d["logits"], K_DEC, SCALE, d["rows"], d["map"], d["shared"], d["residual"],
+                             d["gamma"], d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"],
+                             topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
+        nbf = bytes_router(T, H, E_DEC) + bytes_tail(T, H, K_DEC, E=E_DEC, route_out=True)
+        add("decode layer: router+fused tail", T, H, fusedl, nbf, sets)
         add("decode layer: router+route+finalize", T, H, full, nb, sets)
         add("finalize+shared+residual+RMSNorm", T, H, fin, bytes_tail(T, H, K_DEC), sets)
         del sets
@@ -547,6 +561,45 @@ def run_sweep(torch, M, stream, l2, peak):
         out[-1]["TFLOPs"] = round(2.0 * T * E_DEC * H / (out[-1]["us"] * 1e-6) / 1e12, 1)
         del sets
         torch.cuda.empty_cache()
+    # E = 168, the real checkpoint's expert count, beside the E = 256 rows
+    for T in [64, 8192]:
+        H, E = H_DEC, 168
+        k = K_DEC if T == 64 else 1
+        nb = bytes_router(T, H, E)
+        nbl = nb + (bytes_tail(T, H, K_DEC, E=E, route_out=True) if T == 64 else 0)
+        sets = [device_layer(T, H, E, k, seed=9700 + i, shared=T == 64, router=True, scale=SCALE)
+                for i in range(nsets_for(nbl))]
+        torch.cuda.synchronize()
+
+        def rtr(d):
+            M.moe_router_logits_fp32(d["x"], d["w_gate"], logits_out=d["logits"], stream=s)
+        add("router GEMM E=168 (BF16 -> FP32 logits)", T, H, rtr, nb, sets)
+        out[-1]["TFLOPs"] = round(2.0 * T * E * H / (out[-1]["us"] * 1e-6) / 1e12, 1)
+        if T == 64:
+            def layer168(d):
+                rtr(d)
+                M.moe_tail_fused(d["logits"], K_DEC, SCALE, d["rows"], d["map"], d["shared"], d["residual"],
+                                 d["gamma"], d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"],
+                                 topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
+            add("decode layer E=168: router+fused tail", T, H, layer168, nbl, sets)
+        del sets
+        torch.cuda.empty_cache()
+    # rows in the expert-grouped layout an expert GEMM writes (groups padded to
+    # 128 rows) instead of a random permutation: same bytes, other addresses
+    T, H = 2048, 6144
+    nb = bytes_tail(T, H, K_DEC)
+    sets = [device_layer(T, H, E_DEC, K_DEC, seed=9800 + i, scale=SCALE, router=False, logits=True,
+                         map_layout="expert_sorted", expert_block=128) for i in range(nsets_for(nb))]
+    torch.cuda.synchronize()
+    for d in sets:
+        M.moe_topk_route(d["logits"], K_DEC, SCALE, topk_ids=d["topk_ids"], topk_w=d["topk_w"], stream=s)
+
+    def fin_sorted(d):
+        M.moe_finalize_add_rmsnorm(d["rows"], d["map"], d["topk_w"], d["shared"], d["residual"], d["gamma"],
+                                   d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"], stream=s)
+    add("finalize+shared+residual+RMSNorm, expert-grouped rows", T, H, fin_sorted, nb, sets)
+    del sets
+    torch.cuda.empty_cache()
     # row-parallel partials: R=4 local partial buffers replace gather + shared
     for T in [1, 64, 2048]:
         H = 6144
@@ -631,8 +684,8 @@ def run_reference(args):
 
 def run_ncu_case(case):
     """Small cases for ncu captures (a few hundred MB, more than the L2):
-    decode -- 12 layers at T=64 (162 MB), router -> route -> finalize on each
-    layer, twice; prefill -- 2 sets at T=2048 (605 MB), route, finalize and the
+    decode -- 12 layers at T=64 (162 MB), router -> route -> finalize -> fused
+    tail on each layer, twice; prefill -- 2 sets at T=2048 (605 MB), route, finalize and the
     router-less fused tail on each set, twice; router -- the router GEMM on 2
     inputs at T=8192 (x 100 MB each), twice."""
     import torch
@@ -661,6 +714,10 @@ def run_ncu_case(case):
             M.moe_topk_route(d["logits"], K_DEC, SCALE, topk_ids=d["topk_ids"], topk_w=d["topk_w"])
             M.moe_finalize_add_rmsnorm(d["rows"], d["map"], d["topk_w"], d["shared"], d["residual"], d["gamma"],
                                        d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"])
+            if case == "decode":
+                M.moe_tail_fused(d["logits"], K_DEC, SCALE, d["rows"], d["map"], d["shared"], d["residual"],
+                                 d["gamma"], d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"],
+                                 topk_ids=d["topk_ids"], topk_w=d["topk_w"])
             if case == "prefill":
                 M.moe_tail_fused(d["logits"], K_DEC, SCALE, d["rows"], d["map"], d["shared"], d["residual"],
                                  d["gamma"], d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"],

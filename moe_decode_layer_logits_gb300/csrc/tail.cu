@@ -109,6 +109,18 @@ tail_kernel(const TailParams p) {
     sh[m] = (p.shared && vok[m]) ? ld_stream16(p.shared + off) : make_uint4(0, 0, 0, 0);
     res[m] = vok[m] ? ld_stream16(p.residual + off) : make_uint4(0, 0, 0, 0);
   }
+  // gamma too (up to 2 vectors a thread): otherwise its load would be the
+  // last dependent round trip, after the reductions
+  constexpr bool kEarlyGamma = VPT <= 2;
+  float4 gam[kEarlyGamma ? 2 * VPT : 1];
+  if constexpr (kEarlyGamma) {
+#pragma unroll
+    for (int m = 0; m < VPT; ++m) {
+      const float4* g4 = reinterpret_cast<const float4*>(p.gamma + static_cast<int64_t>(vidx[m]) * 8);
+      gam[2 * m] = vok[m] ? __ldg(g4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      gam[2 * m + 1] = vok[m] ? __ldg(g4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
 
   // -- slot table: map entries (checked) and, without routing, the weights
   if (tid < k) {
@@ -242,8 +254,15 @@ tail_kernel(const TailParams p) {
 #pragma unroll
   for (int m = 0; m < VPT; ++m) {
     if (!vok[m]) continue;
-    const float4* g4 = reinterpret_cast<const float4*>(p.gamma + static_cast<int64_t>(vidx[m]) * 8);
-    const float4 g0 = __ldg(g4), g1 = __ldg(g4 + 1);
+    float4 g0, g1;
+    if constexpr (kEarlyGamma) {
+      g0 = gam[2 * m];
+      g1 = gam[2 * m + 1];
+    } else {
+      const float4* g4 = reinterpret_cast<const float4*>(p.gamma + static_cast<int64_t>(vidx[m]) * 8);
+      g0 = __ldg(g4);
+      g1 = __ldg(g4 + 1);
+    }
     uint4 o;
     o.x = pack_bf16x2(acc[m][0] * inv * g0.x, acc[m][1] * inv * g0.y);
     o.y = pack_bf16x2(acc[m][2] * inv * g0.z, acc[m][3] * inv * g0.w);
@@ -257,14 +276,15 @@ tail_kernel(const TailParams p) {
 // Large batches: a persistent kernel fed by bulk copies (TMA).
 //
 // One CTA per SM walks the tokens t = blockIdx.x, + gridDim.x, ...
-//  - warp 0 (producer): lane j copies slot j's expert-row piece (then the
-//    shared, partial and residual pieces) of one chunk of H into a ring of
+//  - warp 0 (producer): copies the shared, partial and residual pieces, then
+//    (lane j) slot j's expert-row piece, of one chunk of H into a ring of
 //    shared-memory stages with cp.async.bulk, counted on the stage's "full"
-//    mbarrier; the next token's map entries are prefetched while copies fly;
+//    mbarrier; map entries are loaded a token ahead and the next token's rows
+//    requested into the L2;
 //  - warp 1 (weights): per token, the routing weights -- loaded, or routed
 //    from the logits (router-less variant) -- into a ring of token slots, up
 //    to kWRing tokens ahead of the consumers; unusable map entries get 0;
-//  - warps 2..9 (consumers): FP32 accumulation in the same order as
+//  - warps 2..13 (consumers): FP32 accumulation in the same order as
 //    tail_kernel, residual_out stored per chunk, the token's r kept in
 //    registers across chunks until the sum of squares is reduced, then the
 //    normalised row stored.  Each consumer warp releases a stage ("empty")
@@ -521,6 +541,19 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
     const int ct = tid - 64, cw = warp - 2;
     const int ncv = sh.chunk >> 3;  // vectors per chunk
     float rr[VPT][8];
+    // gamma of this thread's vectors, the same for every token: loaded once
+    // (up to 2 vectors a thread; wider rows load it per token)
+    constexpr bool kGammaRegs = VPT <= 2;
+    float4 gam[kGammaRegs ? 2 * VPT : 1];
+    if constexpr (kGammaRegs) {
+#pragma unroll
+      for (int m = 0; m < VPT; ++m) {
+        const int v = ct + m * kStreamConsumers;
+        const float4* g4 = reinterpret_cast<const float4*>(p.gamma + static_cast<int64_t>(v) * 8);
+        gam[2 * m] = v < nvec ? __ldg(g4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        gam[2 * m + 1] = v < nvec ? __ldg(g4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
     for (int i = 0; i < ntok; ++i) {
       const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(i) * G;
       const int64_t roff = t * H;
@@ -599,8 +632,15 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
       for (int m = 0; m < VPT; ++m) {
         const int v = ct + m * kStreamConsumers;
         if (v >= nvec) continue;
-        const float4* g4 = reinterpret_cast<const float4*>(p.gamma + static_cast<int64_t>(v) * 8);
-        const float4 g0 = __ldg(g4), g1 = __ldg(g4 + 1);
+        float4 g0, g1;
+        if constexpr (kGammaRegs) {
+          g0 = gam[2 * m];
+          g1 = gam[2 * m + 1];
+        } else {
+          const float4* g4 = reinterpret_cast<const float4*>(p.gamma + static_cast<int64_t>(v) * 8);
+          g0 = __ldg(g4);
+          g1 = __ldg(g4 + 1);
+        }
         uint4 o;
         o.x = pack_bf16x2(rr[m][0] * inv * g0.x, rr[m][1] * inv * g0.y);
         o.y = pack_bf16x2(rr[m][2] * inv * g0.z, rr[m][3] * inv * g0.w);

@@ -218,6 +218,12 @@ FIN = [  # name, T, H, E, k, extra kwargs
     ("stream-half-round", 380, 6144, 256, 8, dict(seed=24)),
     ("stream-rem-over-half", 400, 6144, 64, 8, dict(seed=25, shared=False)),
     ("stream-3-chunks", 330, 8192, 64, 4, dict(seed=26, R=3)),
+    # the final-norm form (no routed part, no shared expert: RMSNorm of the
+    # residual) and expert-grouped row layouts with padded groups
+    ("final-norm", 9, 6144, 16, 0, dict(seed=27, shared=False)),
+    ("stream-final-norm", 320, 6144, 16, 0, dict(seed=30, shared=False)),
+    ("expert-sorted-decode", 64, 6144, 256, 8, dict(seed=28, map_layout="expert_sorted", expert_block=8)),
+    ("stream-expert-sorted", 400, 6144, 256, 8, dict(seed=29, map_layout="expert_sorted", expert_block=64)),
 ]
 
 
@@ -336,6 +342,9 @@ FUSED = [  # name, T, H, E, k, kw
     ("e1", 3, 64, 1, 1, dict(seed=10)),
     ("stream-e1024", 320, 1024, 1024, 32, dict(seed=11)),
     ("stream-ragged", 400, 2056, 72, 3, dict(seed=12, shared=False)),
+    # the real checkpoint's 168 experts, and an expert-grouped row layout
+    ("decode-64-e168", 64, 6144, 168, 8, dict(seed=13)),
+    ("stream-e168-expert-sorted", 400, 6144, 168, 8, dict(seed=14, map_layout="expert_sorted", expert_block=128)),
 ]
 
 
