@@ -153,6 +153,19 @@ int moe_tail_fused(const float* logits, int64_t E, int32_t k, float routed_scale
                    int32_t* topk_ids_out, float* topk_w_out,
                    int64_t T, int64_t H, int32_t* err_flag, cudaStream_t stream);
 
+/*
+ * Test hook of the bounded waits; no counterpart on the pages.  The next
+ * launch of the persistent tail kernel (the path taken by batches of at
+ * least two tokens per SM) leaves stage `stage` of its first CTA unarmed and
+ * uncopied, so that CTA's consumers wait for it until their bounded wait
+ * runs out (about two seconds), set MOE_FLAG_TIMEOUT in err_flag and stop
+ * waiting; the launch still completes, its outputs are invalid, and the next
+ * launch is unaffected.  One launch takes the request (a decode-size launch
+ * leaves it for the next persistent one); stage -1 cancels it.  Returns
+ * MOE_OK, or MOE_ERR_INVALID_ARG for stage < -1.  Not for production use.
+ */
+int moe_debug_withhold_stream_stage(int32_t stage);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,6 +20,7 @@ from . import _lib
 from ._lib import MoeTailError, check, lib
 
 __all__ = [
+    "moe_debug_withhold_stream_stage",
     "moe_router_logits_fp32",
     "moe_topk_route",
     "moe_finalize_add_rmsnorm",
@@ -129,3 +130,10 @@ def moe_tail_fused(logits, k, routed_scale, rows, row_map, shared, residual, gam
         T, H, _ptr(err_flag, torch.int32, "err_flag", optional=True), _stream(stream))
     check(st, "moe_tail_fused")
     return residual_out, normed_out, topk_ids, topk_w
+
+
+def moe_debug_withhold_stream_stage(stage):
+    """Test hook of the bounded waits: the next persistent-kernel launch
+    leaves stage `stage` of its first CTA uncopied, so that CTA's wait runs
+    out and MOE_FLAG_TIMEOUT is set; -1 cancels the request."""
+    check(lib().moe_debug_withhold_stream_stage(int(stage)), "moe_debug_withhold_stream_stage")

@@ -18,6 +18,7 @@ MOE_ERR_MISALIGNED = 3
 MOE_ERR_CUDA = 4
 MOE_ERR_BAD_INDEX = 5
 MOE_FLAG_BAD_INDEX = 1
+MOE_FLAG_TIMEOUT = 2
 MOE_MAX_E = 1024
 MOE_MAX_K = 32
 MOE_MAX_R = 8
@@ -35,6 +36,7 @@ SIGNATURES = {
                                                 _vp, _vp, _i64, _i64, _vp, _vp]),
     "moe_tail_fused": (ctypes.c_int, [_vp, _i64, _i32, _f32, _vp, _i64, _vp, _vp, _vp, _vp, _f32, _vp, _vp,
                                       _vp, _vp, _i64, _i64, _vp, _vp]),
+    "moe_debug_withhold_stream_stage": (ctypes.c_int, [_i32]),
 }
 
 _lib = None

@@ -12,6 +12,8 @@
 // block size so that every load instruction of a warp covers 512 contiguous
 // bytes.  The k expert rows of a token are gathered KB slots at a time, with
 // all of a batch's loads issued before the first FMA.
+#include <atomic>
+
 #include "host_util.h"
 #include "route.cuh"
 
@@ -312,6 +314,7 @@ struct StreamShape {
   int rows;         // row pieces per stage: k slots, shared, R partials, residual
   int stage_bytes;  // rows * chunk * 2 rounded up to 128
   int ahead;        // 0..kMaxAhead: tokens prefetched into the L2 ahead of the one being copied
+  int withhold;     // test hook: the stage CTA 0 never copies (its consumers' wait runs out), or -1
 };
 
 __device__ __forceinline__ bool stream_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -445,27 +448,34 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
                     ? p.map[(static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(q) * G) * k + lane]
                     : -1;
     int issued = 0;
-    for (int i = 0; i < ntok && !*abort_v; ++i) {
+    const int withheld = blockIdx.x == 0 ? sh.withhold : -1;
+    bool stop = false;
+    for (int i = 0; i < ntok && !stop; ++i) {
       const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(i) * G;
       int row_cur = -1;
       for (int c = 0; c < sh.nchunks; ++c) {
         const int u = i * sh.nchunks + c, s = u % sh.nstages, n = u / sh.nstages;
-        if (n > 0 && !stream_wait(&empty_bar[s], (n - 1) & 1, abort_v, p.err_flag)) break;
+        if ((n > 0 && !stream_wait(&empty_bar[s], (n - 1) & 1, abort_v, p.err_flag)) || *abort_v) {
+          stop = true;  // no stage is armed after an abort
+          break;
+        }
         const int c0 = c * sh.chunk;
         const int clen = min(sh.chunk, H - c0);
-        if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(sh.rows * clen * 2));
-        __syncwarp();
-        unsigned char* st = stage_mem + static_cast<size_t>(s) * sh.stage_bytes;
-        // the pieces that do not depend on the map go first: they fly while
-        // the token's first map entries may still be loading
-        for (int l = k + lane; l < sh.rows; l += 32)
-          bulk_copy_g2s(st + static_cast<size_t>(l) * sh.chunk * 2, stream_piece(p, t, l, sh.rows, -1) + c0,
-                        static_cast<uint32_t>(clen * 2), &full_bar[s], pol);
         if (c == 0 && lane < k) row_cur = checked_entry(p, mrow[0]);
-        if (lane < k)
-          bulk_copy_g2s(st + static_cast<size_t>(lane) * sh.chunk * 2,
-                        stream_piece(p, t, lane, sh.rows, row_cur) + c0, static_cast<uint32_t>(clen * 2),
-                        &full_bar[s], pol);
+        if (u != withheld) {  // a withheld stage is neither armed nor copied: its full wait runs out
+          if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(sh.rows * clen * 2));
+          __syncwarp();
+          unsigned char* st = stage_mem + static_cast<size_t>(s) * sh.stage_bytes;
+          // the pieces that do not depend on the map go first: they fly while
+          // the token's first map entries may still be loading
+          for (int l = k + lane; l < sh.rows; l += 32)
+            bulk_copy_g2s(st + static_cast<size_t>(l) * sh.chunk * 2, stream_piece(p, t, l, sh.rows, -1) + c0,
+                          static_cast<uint32_t>(clen * 2), &full_bar[s], pol);
+          if (lane < k)
+            bulk_copy_g2s(st + static_cast<size_t>(lane) * sh.chunk * 2,
+                          stream_piece(p, t, lane, sh.rows, row_cur) + c0, static_cast<uint32_t>(clen * 2),
+                          &full_bar[s], pol);
+        }
         issued = u + 1;
         if (c == 0) {
           // the L2 prefetch window: tokens i+1..i+ahead are requested once
@@ -490,6 +500,7 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
     // drain: no copy may land after this CTA exits
     if (lane == 0) {
       for (int u = issued > sh.nstages ? issued - sh.nstages : 0; u < issued; ++u) {
+        if (u == withheld) continue;
         for (int it = 0; it < kMaxProbes; ++it)
           if (mbar_try_wait(&full_bar[u % sh.nstages], (u / sh.nstages) & 1, kProbeHintNs)) break;
       }
@@ -725,6 +736,7 @@ static bool stream_shape(int H, int rows, StreamShape& sh) {
       sh.rows = rows;
       sh.stage_bytes = stage;
       sh.ahead = 1;
+      sh.withhold = -1;
       return true;
     }
   }
@@ -771,6 +783,11 @@ static bool use_stream(int64_t T, int H, int rows, int nsm, StreamShape& sh) {
   return T >= 2 * static_cast<int64_t>(nsm) && H / 8 <= 4 * kStreamConsumers && stream_shape(H, rows, sh);
 }
 
+// Test hook of the bounded waits (moe_debug_withhold_stream_stage): a stage
+// that the next persistent-kernel launch withholds, taken by that launch.
+static std::atomic<int> g_withheld_stage{-1};
+static int take_withheld_stage() { return g_withheld_stage.exchange(-1); }
+
 template <bool ROUTE>
 static int launch_tail(TailParams p, int64_t T, cudaStream_t stream) {
   const int nsm = sm_count();
@@ -796,6 +813,7 @@ static int launch_tail(TailParams p, int64_t T, cudaStream_t stream) {
       const int grid = Tc < nsm ? Tc : nsm;
       // one token of rows requested into the L2 ahead of its copies
       sh.ahead = 1;
+      sh.withhold = t0 == 0 ? take_withheld_stage() : -1;
       const int vpt = (p.H / 8 + kStreamConsumers - 1) / kStreamConsumers;
       if (!ROUTE) e = launch_stream_e<0>(q, Tc, sh, grid, vpt, stream);
       else if (p.E <= 256) e = launch_stream_e<8>(q, Tc, sh, grid, vpt, stream);
@@ -907,4 +925,10 @@ extern "C" int moe_tail_fused(const float* logits, int64_t E, int32_t k, float r
   p.ids_out = topk_ids_out;
   p.w_out = topk_w_out;
   return launch_tail<true>(p, T, stream);
+}
+
+extern "C" int moe_debug_withhold_stream_stage(int32_t stage) {
+  if (stage < -1) return MOE_ERR_INVALID_ARG;
+  moe::g_withheld_stage.store(stage);
+  return MOE_OK;
 }

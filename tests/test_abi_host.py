@@ -184,6 +184,12 @@ def test_fused_argument_checks(lib, kw, want):
     assert lib.moe_tail_fused(*fused(**kw), S) == want
 
 
+def test_withhold_hook_argument_check(lib):
+    # host-only: the request is stored for the next persistent-kernel launch
+    assert lib.moe_debug_withhold_stream_stage(-2) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_debug_withhold_stream_stage(-1) == L.MOE_OK
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     import moe_decode_layer_logits_gb300 as M

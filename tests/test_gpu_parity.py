@@ -282,6 +282,26 @@ def test_finalize_bad_index_sets_flag_and_reads_zero(M, T):
     assert int(flag.item()) == 0
 
 
+def test_stream_wait_runs_out_and_the_next_launch_is_clean(M):
+    """The persistent kernel's bounded waits: with one stage withheld (test
+    hook), the waiting CTA gives up after about two seconds, the launch
+    completes with the timeout bit set, and the next launch is correct."""
+    import moe_decode_layer_logits_gb300._lib as L
+    c = tail_case(400, 2048, 64, 8, router=False, seed=31)  # >= 2 tokens per SM: the persistent kernel
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    M.moe_debug_withhold_stream_stage(1)
+    _run_finalize(M, c, err_flag=flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) & L.MOE_FLAG_TIMEOUT
+    flag.zero_()
+    ro, no = _run_finalize(M, c, err_flag=flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 0
+    _check_tail(c, _oracle_tail(c), ro, no, tag="after-timeout")
+    with pytest.raises(L.MoeTailError):
+        M.moe_debug_withhold_stream_stage(-2)
+
+
 def test_finalize_is_deterministic(M):
     c = tail_case(64, 6144, 256, 8, router=False, seed=23)
     a = _run_finalize(M, c)
