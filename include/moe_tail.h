@@ -22,7 +22,8 @@
  * Conventions for every entry point:
  *  - Pointers are DEVICE pointers unless stated otherwise.  The caller owns
  *    every buffer; the library allocates nothing and keeps no state beyond
- *    cached device attributes (SM count) per device.
+ *    cached device attributes (SM count) per device and the one-shot request
+ *    of the test hook at the end of this header.
  *  - Tensors are row-major with the last dimension contiguous.  BF16 data is
  *    passed as `const void*` holding IEEE bfloat16 bit patterns.
  *  - Work is enqueued on `stream` (which may be 0, the legacy default stream)
@@ -125,6 +126,9 @@ int moe_topk_route(const float* logits, int32_t* topk_ids, float* topk_w,
  *                 never dereferenced: its row counts as zero and, if err_flag
  *                 is given, MOE_FLAG_BAD_INDEX is OR-ed into *err_flag (the
  *                 caller clears it and reads it after the stream completes).
+ *                 MOE_FLAG_TIMEOUT there means a pipeline wait of the
+ *                 large-batch kernel ran out and that launch's outputs are
+ *                 invalid.
  *   0 <= k <= MOE_MAX_K (k == 0: no routed part; rows/map/topk_w may be NULL);
  *   0 <= R <= MOE_MAX_R; H >= 8, H % 8 == 0, H <= 65536; eps >= 0 and finite.
  */
