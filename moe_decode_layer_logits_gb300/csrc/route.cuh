@@ -35,17 +35,31 @@ __device__ __forceinline__ float route_unkey(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Load a token's logits row (global memory, E <= 32 * EPL) as keys; lane l
-// gets experts l, l + 32, ...  Split from the selection so that callers can
-// issue the loads early.
+// Load a token's logits row (global memory, E <= 32 * EPL); lane l gets
+// experts l, l + 32, ...  The raw bits are loaded where this is called (the
+// loads are not moved towards their first use) and turned into keys by
+// route_select, so a caller can issue them early and keep working while they
+// fly.  Slots past E hold a marker that route_select turns into key 0.
 template <int EPL>
 __device__ __forceinline__ void route_load_keys(const float* __restrict__ row, int E, uint32_t (&key)[EPL]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int s = 0; s < EPL; ++s) {
     const int i = lane + 32 * s;
-    key[s] = i < E ? route_key(__ldg(row + i)) : 0u;
+    if (i < E) {
+      asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(key[s]) : "l"(row + i));
+    } else {
+      key[s] = 0xFFFFFFFFu;  // a NaN pattern no finite logit has
+    }
   }
+}
+
+// Raw logit bits (route_load_keys) -> order-preserving keys; the past-E
+// marker becomes 0.
+template <int EPL>
+__device__ __forceinline__ void route_bits_to_keys(uint32_t (&key)[EPL]) {
+#pragma unroll
+  for (int s = 0; s < EPL; ++s) key[s] = key[s] == 0xFFFFFFFFu ? 0u : route_key(__uint_as_float(key[s]));
 }
 
 // Compare-exchange leaving the larger value in `a`.
@@ -102,13 +116,15 @@ __device__ __forceinline__ void route_top8(const uint32_t (&key)[EPL], uint64_t 
   }
 }
 
-// Select the top k (1 <= k <= min(E, 32)) of the keys held by the warp and
-// weight them.  All 32 lanes call this; lane j < k receives the j-th
-// selected expert in `id` and its weight in `w`.  Consumes `key`.  NETWORK
+// Select the top k (1 <= k <= min(E, 32)) of the logits loaded by
+// route_load_keys and weight them.  All 32 lanes call this; lane j < k
+// receives the j-th selected expert in `id` and its weight in `w`.  Consumes
+// `key`.  NETWORK
 // picks the merge network where it applies (k <= 8, EPL <= 8).
 template <int EPL, bool NETWORK>
 __device__ __forceinline__ void route_select(uint32_t (&key)[EPL], int k, float scale, int& id, float& w) {
   const int lane = threadIdx.x & 31;
+  route_bits_to_keys<EPL>(key);
   uint32_t my_key = 0u;
   int my_id = 0;
   int rounds = k;
