@@ -533,11 +533,10 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
         prefetch_row_l2(p.logits + (t + static_cast<int64_t>(kLogitsAhead) * G) * p.E, p.E);
       if (ROUTE) {
         int id;
-        // the first token is on every consumer's critical path (the shorter
-        // dependency chain of the merge network); later ones run ahead of the
-        // consumers (the fewer instructions of the rounds)
-        if (i == 0) route_select<KEYS, true>(keys_nxt, k, p.scale, id, w);
-        else route_select<KEYS, false>(keys_nxt, k, p.scale, id, w);
+        // the rounds (fewer instructions): this warp runs ahead of the
+        // consumers, its loads issued a token early (measured: 1% faster
+        // than the merge network for the first token)
+        route_select<KEYS, false>(keys_nxt, k, p.scale, id, w);
         if (lane < k) {
           if (p.ids_out) p.ids_out[t * k + lane] = id;
           if (p.w_out) p.w_out[t * k + lane] = w;
