@@ -108,23 +108,30 @@ __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Sum of one float per CTA over the thread-block cluster.  Every CTA writes
-// its value into slot[rank] of every peer (distributed shared memory), one
-// barrier publishes the stores, and each CTA adds its local slots in rank
-// order, so all CTAs agree bit for bit.  The caller has arrived on the
+// Sum of one float per thread over the whole thread-block cluster, in one
+// exchange: every warp pushes its sum into slot [rank * nwarps + warp] of
+// every CTA (distributed shared memory), one barrier publishes the stores,
+// and each thread adds the cluster size x nwarps slots in that fixed order,
+// so all CTAs get the same total, bit for bit.  The caller has arrived on the
 // cluster barrier once (cluster_arrive_relaxed) since the kernel started;
-// every thread of every CTA in the cluster must call this.
-__device__ __forceinline__ float cluster_sum(float cta_value, float* slots) {
+// every thread of every CTA in the cluster must call this.  `slots` holds at
+// least cluster size x nwarps floats.
+__device__ __forceinline__ float cluster_block_sum(float v, float* slots) {
   cg::cluster_group cluster = cg::this_cluster();
   const unsigned n = cluster.num_blocks();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  v = warp_sum(v);
   cluster_wait_acquire();  // every peer has started: its shared memory is live
-  if (threadIdx.x < n) *cluster.map_shared_rank(slots + cluster.block_rank(), threadIdx.x) = cta_value;
+  if (static_cast<unsigned>(lane) < n)
+    *cluster.map_shared_rank(slots + cluster.block_rank() * nwarps + warp, lane) = v;
   cluster_arrive_release();
   cluster_wait_acquire();
   float s = 0.f;
-  for (unsigned r = 0; r < n; ++r) s += slots[r];
+  for (int i = 0; i < static_cast<int>(n) * nwarps; ++i) s += slots[i];
   return s;
 }
+
 
 }  // namespace moe
 

@@ -56,7 +56,7 @@ tail_kernel(const TailParams p) {
   __shared__ int map_s[MOE_MAX_K];
   __shared__ float w_s[MOE_MAX_K];
   __shared__ float red[33];
-  __shared__ float cluster_slots[8];
+  __shared__ float cluster_slots[8 * (kMaxThreads / 32)];  // [cluster rank][warp]
 
   const int t = blockIdx.y;
   const int tid = threadIdx.x;
@@ -250,8 +250,9 @@ tail_kernel(const TailParams p) {
     }
   }
 
-  ss = block_sum(ss, red);
-  if (cs > 1) ss = cluster_sum(ss, cluster_slots);
+  // sum of squares over the token's row: the block, then the cluster (one
+  // exchange of warp sums when the row is split over a cluster)
+  ss = cs > 1 ? cluster_block_sum(ss, cluster_slots) : block_sum(ss, red);
   const float inv = rsqrtf(ss / static_cast<float>(p.H) + p.eps);
 
   // -- RMSNorm output
