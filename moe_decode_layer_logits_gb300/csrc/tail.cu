@@ -90,7 +90,17 @@ tail_kernel(const TailParams p) {
   }
   grid_dependency_wait();
 
-  // router-less variant: warp 0 requests the token's logits first, so the
+  // the slot table's loads go first (every row gather waits for them),
+  // pinned here and consumed at the slot table below
+  int map_raw = -1;
+  uint32_t w_raw = 0u;
+  if (tid < k) {
+    const int32_t* mp = p.map + static_cast<int64_t>(t) * k + tid;
+    asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(map_raw) : "l"(mp));
+    if (!ROUTE) asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(w_raw) : "l"(p.topk_w + static_cast<int64_t>(t) * k + tid));
+  }
+
+  // router-less variant: warp 0 requests the token's logits next, so the
   // selection below overlaps the expert-row gathers
   constexpr int KEYS = EPL > 0 ? EPL : 1;
   uint32_t keys[KEYS];
@@ -128,13 +138,13 @@ tail_kernel(const TailParams p) {
 
   // -- slot table: map entries (checked) and, without routing, the weights
   if (tid < k) {
-    int m = p.map[static_cast<int64_t>(t) * k + tid];
+    int m = map_raw;
     if (m < 0 || static_cast<int64_t>(m) >= p.n_rows) {
       if (p.err_flag) atomicOr(p.err_flag, MOE_FLAG_BAD_INDEX);
       m = -1;  // never dereferenced; the row counts as zero
     }
     map_s[tid] = m;
-    if (!ROUTE) w_s[tid] = p.topk_w[static_cast<int64_t>(t) * k + tid];
+    if (!ROUTE) w_s[tid] = __uint_as_float(w_raw);
   }
   __syncthreads();
 
