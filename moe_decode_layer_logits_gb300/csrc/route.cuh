@@ -4,19 +4,15 @@
 // Details: the router folds the routed scaling factor into the weights).
 //
 // Lane l holds the logits of experts l, l + 32, ... as order-preserving
-// integer keys in registers.  Two selection schemes give the same result:
-//  - rounds (any k): each of the k rounds scans the lane's keys (the first
-//    maximum wins, i.e. the lowest expert of the lane), then two warp
-//    reductions pick the largest key and, among lanes holding it, the lowest
-//    expert index; the winner clears its key;
-//  - a merge network (k <= 8, at most 8 keys per lane): each lane sorts its
-//    candidates, packed as (key, inverted expert index) so that one 64-bit
-//    order ranks by logit and then by lower expert, and five butterfly steps
-//    merge the lanes' sorted top-8 lists until every lane holds the warp's.
-// The rounds issue fewer instructions (better where many warps share an SM);
-// the network has the shorter dependency chain (better when one token's
-// routing is on the critical path).  Key 0 marks a taken or padding slot:
-// every finite logit has a key >= 1.
+// integer keys in registers, and the k experts are taken in k rounds.  With
+// at most 8 keys per lane, each lane first sorts its keys (descending, lower
+// expert first among equal keys, one 64-bit order on (key, inverted slot)),
+// and each round takes one warp max over the lanes' heads and a ballot of the
+// lanes holding it; a second reduction picks the lowest expert only when
+// several lanes tie; the winner pops its head.  Wider rows scan the lane's
+// keys each round, then two reductions pick the largest key and the lowest
+// expert holding it, and the winner clears its key.  Key 0 marks a taken or
+// padding slot: every finite logit has a key >= 1.
 #pragma once
 
 #include "common.cuh"
@@ -69,79 +65,60 @@ __device__ __forceinline__ void cx_desc(uint64_t& a, uint64_t& b) {
   a = hi;
 }
 
-// The warp's 8 largest packed candidates, sorted descending, in every lane.
-// Lane l contributes experts l + 32 s (s < EPL <= 8).
-template <int EPL>
-__device__ __forceinline__ void route_top8(const uint32_t (&key)[EPL], uint64_t (&v)[8]) {
-  static_assert(EPL >= 1 && EPL <= 8, "the merge network holds 8 candidates per lane");
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int s = 0; s < 8; ++s)
-    v[s] = s < EPL ? (static_cast<uint64_t>(key[s < EPL ? s : 0]) << 32) |
-                         static_cast<uint32_t>(~(lane + 32 * s))
-                   : 0ull;
-  // bitonic sort of the lane's 8 candidates, descending
-#pragma unroll
-  for (int size = 2; size <= 8; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int j = i ^ stride;
-        if (j > i) {
-          if ((i & size) == 0) cx_desc(v[i], v[j]);
-          else cx_desc(v[j], v[i]);
-        }
-      }
-    }
-  }
-  // merge with the partner lane's list: the top 8 of two descending lists a,
-  // b are max(a[i], b[7 - i]) (a bitonic sequence), sorted by three steps
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    uint64_t m[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, v[7 - i], d);
-      m[i] = v[i] > o ? v[i] : o;
-    }
-#pragma unroll
-    for (int stride = 4; stride > 0; stride >>= 1) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if ((i & stride) == 0) cx_desc(m[i], m[i + stride]);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = m[i];
-  }
-}
-
 // Select the top k (1 <= k <= min(E, 32)) of the logits loaded by
 // route_load_keys and weight them.  All 32 lanes call this; lane j < k
 // receives the j-th selected expert in `id` and its weight in `w`.  Consumes
-// `key`.  NETWORK
-// picks the merge network where it applies (k <= 8, EPL <= 8).
-template <int EPL, bool NETWORK>
+// `key`.
+template <int EPL>
 __device__ __forceinline__ void route_select(uint32_t (&key)[EPL], int k, float scale, int& id, float& w) {
   const int lane = threadIdx.x & 31;
   route_bits_to_keys<EPL>(key);
   uint32_t my_key = 0u;
   int my_id = 0;
   int rounds = k;
-  if constexpr (NETWORK && EPL <= 8) {
-    if (k <= 8) {
-      uint64_t v[8];
-      route_top8<EPL>(key, v);
-      uint64_t mine = 0ull;
+  if constexpr (EPL <= 8) {
+    if (rounds > 0) {
+      // Sorted heads: each lane sorts its candidates once (descending key,
+      // ascending slot among equal keys), then every round needs one warp
+      // max over the lanes' heads and a ballot; only when several lanes tie
+      // on that key does a second reduction pick the lowest expert.
+      uint64_t v[EPL];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i == lane) mine = v[i];
-      my_key = static_cast<uint32_t>(mine >> 32);
-      my_id = static_cast<int>(~static_cast<uint32_t>(mine));
+      for (int s = 0; s < EPL; ++s)
+        v[s] = (static_cast<uint64_t>(key[s]) << 32) | static_cast<uint32_t>(0xFFFF - s);
+#pragma unroll
+      for (int size = 2; size <= EPL; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+          for (int i = 0; i < EPL; ++i) {
+            const int j = i ^ stride;
+            if (j > i) {
+              if ((i & size) == 0) cx_desc(v[i], v[j]);
+              else cx_desc(v[j], v[i]);
+            }
+          }
+        }
+      }
+      for (int round = 0; round < rounds; ++round) {
+        const uint32_t head = static_cast<uint32_t>(v[0] >> 32);
+        const uint32_t hexp = static_cast<uint32_t>(lane + 32 * (0xFFFF - static_cast<int>(v[0] & 0xFFFFu)));
+        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, head);
+        const uint32_t tied = __ballot_sync(0xFFFFFFFFu, head == m);
+        const uint32_t win = (tied & (tied - 1u)) == 0u
+                                 ? __shfl_sync(0xFFFFFFFFu, hexp, __ffs(tied) - 1)
+                                 : __reduce_min_sync(0xFFFFFFFFu, head == m ? hexp : 0xFFFFFFFFu);
+        if (static_cast<int>(win & 31u) == lane) {  // the winner pops its head
+#pragma unroll
+          for (int i = 0; i + 1 < EPL; ++i) v[i] = v[i + 1];
+          v[EPL - 1] = 0ull;
+        }
+        if (lane == round) { my_key = m; my_id = static_cast<int>(win); }
+      }
       rounds = 0;
     }
   }
-  for (int round = 0; round < rounds; ++round) {
+  for (int round = 0; round < rounds; ++round) {  // wider rows: scan the lane's keys each round
     uint32_t bk = 0u;
     int bs = 0;
 #pragma unroll
@@ -170,12 +147,12 @@ __device__ __forceinline__ void route_select(uint32_t (&key)[EPL], int k, float 
 }
 
 // Both phases for one token row.
-template <int EPL, bool NETWORK>
+template <int EPL>
 __device__ __forceinline__ void warp_route(const float* __restrict__ row, int E, int k, float scale,
                                            int& id, float& w) {
   uint32_t key[EPL];
   route_load_keys<EPL>(row, E, key);
-  route_select<EPL, NETWORK>(key, k, scale, id, w);
+  route_select<EPL>(key, k, scale, id, w);
 }
 
 }  // namespace moe

@@ -45,11 +45,9 @@ struct TailParams {
 };
 
 constexpr int kMaxThreads = 256;  // per CTA; VPT <= 4 covers 1024 vectors (16 KB of a row)
-constexpr int kRouteNetMinT = 36;  // decode kernel: merge-network top-k from this batch size
 
-// EPL > 0: route the token from its logits first (E <= 32 * EPL), with the
-// merge network (NET) or the rounds.
-template <int VPT, int KB, int EPL, bool NET>
+// EPL > 0: route the token from its logits first (E <= 32 * EPL).
+template <int VPT, int KB, int EPL>
 __global__ void __launch_bounds__(kMaxThreads)
 tail_kernel(const TailParams p) {
   constexpr bool ROUTE = EPL > 0;
@@ -173,7 +171,7 @@ tail_kernel(const TailParams p) {
       if (tid < 32) {
         int id;
         float w;
-        route_select<KEYS, NET>(keys, k, p.scale, id, w);
+        route_select<KEYS>(keys, k, p.scale, id, w);
         if (tid < k) {
           w_s[tid] = w;
           if (rank == 0) {
@@ -544,10 +542,7 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
         prefetch_row_l2(p.logits + (t + static_cast<int64_t>(kLogitsAhead) * G) * p.E, p.E);
       if (ROUTE) {
         int id;
-        // the rounds (fewer instructions): this warp runs ahead of the
-        // consumers, its loads issued a token early (measured: 1% faster
-        // than the merge network for the first token)
-        route_select<KEYS, false>(keys_nxt, k, p.scale, id, w);
+        route_select<KEYS>(keys_nxt, k, p.scale, id, w);  // runs ahead of the consumers
         if (lane < k) {
           if (p.ids_out) p.ids_out[t * k + lane] = id;
           if (p.w_out) p.w_out[t * k + lane] = w;
@@ -702,7 +697,7 @@ static TailLaunch choose_tail_launch(int64_t T, int H, int nsm) {
   return {cs, vpt, threads};
 }
 
-template <int VPT, int EPL, bool NET>
+template <int VPT, int EPL>
 static cudaError_t launch_tail_v(const TailParams& p, int T, const TailLaunch& L, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.cs, T, 1);
@@ -721,16 +716,16 @@ static cudaError_t launch_tail_v(const TailParams& p, int T, const TailLaunch& L
   }
   cfg.attrs = attr;
   cfg.numAttrs = nattr;
-  return cudaLaunchKernelEx(&cfg, tail_kernel<VPT, 8, EPL, NET>, p);
+  return cudaLaunchKernelEx(&cfg, tail_kernel<VPT, 8, EPL>, p);
 }
 
-template <int EPL, bool NET = false>
+template <int EPL>
 static cudaError_t launch_tail_e(const TailParams& q, int Tc, const TailLaunch& L, cudaStream_t stream) {
   switch (L.vpt) {
-    case 1: return launch_tail_v<1, EPL, NET>(q, Tc, L, stream);
-    case 2: return launch_tail_v<2, EPL, NET>(q, Tc, L, stream);
-    case 3: return launch_tail_v<3, EPL, NET>(q, Tc, L, stream);
-    default: return launch_tail_v<4, EPL, NET>(q, Tc, L, stream);
+    case 1: return launch_tail_v<1, EPL>(q, Tc, L, stream);
+    case 2: return launch_tail_v<2, EPL>(q, Tc, L, stream);
+    case 3: return launch_tail_v<3, EPL>(q, Tc, L, stream);
+    default: return launch_tail_v<4, EPL>(q, Tc, L, stream);
   }
 }
 
@@ -832,12 +827,7 @@ static int launch_tail(TailParams p, int64_t T, cudaStream_t stream) {
       else e = launch_stream_e<32>(q, Tc, sh, grid, vpt, stream);
     } else {
       const TailLaunch L = choose_tail_launch(T, p.H, nsm);
-      // the routing sits on each token's critical path: the merge network's
-      // shorter chain pays from a few dozen tokens on, the rounds' fewer
-      // instructions below (measured on the router + fused tail chain:
-      // rounds faster up to T = 32, the network from T = 40)
       if (!ROUTE) e = launch_tail_e<0>(q, Tc, L, stream);
-      else if (p.E <= 256 && Tc >= kRouteNetMinT) e = launch_tail_e<8, true>(q, Tc, L, stream);
       else if (p.E <= 256) e = launch_tail_e<8>(q, Tc, L, stream);
       else e = launch_tail_e<32>(q, Tc, L, stream);
     }

@@ -18,7 +18,7 @@ topk_route_kernel(const float* __restrict__ logits, int32_t* __restrict__ ids, f
   if (t >= T) return;  // whole warp leaves together; the kernel has no block barrier
   int id;
   float w;
-  warp_route<EPL, false>(logits + static_cast<int64_t>(t) * E, E, k, scale, id, w);
+  warp_route<EPL>(logits + static_cast<int64_t>(t) * E, E, k, scale, id, w);
   if (lane < k) {
     ids[static_cast<int64_t>(t) * k + lane] = id;
     wts[static_cast<int64_t>(t) * k + lane] = w;
