@@ -66,10 +66,15 @@ router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, fl
   if (S > 1) cluster_arrive_relaxed();
   allow_dependent_launch();
   // While the previous kernel finishes: L2 prefetch of this CTA's slice of
-  // the gate weight (a hint; the loads below follow the dependency wait).
-  if (tid < 16 && e0 + tid < E && ce > cb) {
+  // the gate weight and, from the first expert tile, of the token rows of x
+  // (hints; the loads below follow the dependency wait and see the final data
+  // whatever the hint fetched).
+  if (ce > cb) {
     const int h0 = cb * 32, h1 = min(H, ce * 32);
-    prefetch_l2(W + static_cast<int64_t>(e0 + tid) * H + h0, static_cast<uint32_t>((h1 - h0) * 2));
+    if (tid < 16 && e0 + tid < E)
+      prefetch_l2(W + static_cast<int64_t>(e0 + tid) * H + h0, static_cast<uint32_t>((h1 - h0) * 2));
+    else if (blockIdx.x == 0 && tid >= 32 && tid < 32 + 8 * NT && t0 + tid - 32 < T)  // once per slice of x
+      prefetch_l2(x + static_cast<int64_t>(t0 + tid - 32) * H + h0, static_cast<uint32_t>((h1 - h0) * 2));
   }
   grid_dependency_wait();
 
