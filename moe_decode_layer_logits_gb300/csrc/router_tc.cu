@@ -3,14 +3,20 @@
 // tensor memory (lmdeploy pull 4853, Summary: FP32 router logits through a
 // BF16 GEMM).  At T in the thousands the router is a dense contraction near
 // the tensor-core ridge, so it is tiled for tcgen05:
-//  - one CTA per 128-token x BN-expert tile (UMMA M = 128, N = BN);
+//  - one CTA per 128-expert x BNT-token tile: the gate weight is the M side
+//    (UMMA M = 128) and the tokens the N side (N = BNT), so tensor-memory lane
+//    i holds expert i of the tile and column j token j;
 //  - warp 0 streams 64-wide K blocks of both operands with TMA (128-byte
 //    swizzle, out-of-range rows and columns zero-filled) into a 6-stage ring;
-//  - warp 1 allocates BN tensor-memory columns and one lane issues
+//  - warp 1 allocates BNT tensor-memory columns and one lane issues
 //    tcgen05.mma (kind::f16, 4 per K block), releasing each stage with
 //    tcgen05.commit when the MMAs that read it complete;
 //  - warps 2..5 wait for the final commit and read the accumulator with
-//    tcgen05.ld (each warp its 32-lane quarter = 32 tokens), storing FP32 rows.
+//    tcgen05.ld (each warp its 32-lane quarter = 32 experts, 32 tokens per
+//    load) into a [token][expert] tile in the CTA's own (now idle) operand
+//    ring: for one token the 32 lanes hold 32 consecutive experts, so these
+//    writes are free of bank conflicts; the rows then leave as 16-byte
+//    stores, 512 contiguous bytes per warp.
 // Every wait is bounded; a tile whose pipeline gave up is written as NaN so
 // that the failure is visible in the output.
 #include <cuda.h>
@@ -22,20 +28,21 @@
 
 namespace moe {
 
-constexpr int kTcBM = 128;       // tokens per tile (UMMA M)
+constexpr int kTcBM = 128;       // experts per tile (UMMA M)
+constexpr int kTcBNT = 128;      // tokens per tile (UMMA N)
 constexpr int kTcBK = 64;        // K elements per stage: one 128-byte swizzle row
 constexpr int kTcStages = 6;
 constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
 constexpr int kTcMaxWaits = 1 << 21;
-constexpr uint32_t kTcHintNs = 1000;
 
-template <int BN>
+template <int BNT>
 struct TcSmem {
-  uint8_t a[kTcStages][kTcBM * kTcBK * 2];  // 16 KB per stage, 1024-byte aligned
-  uint8_t b[kTcStages][BN * kTcBK * 2];     // BN * 128 bytes per stage
+  uint8_t a[kTcStages][kTcBM * kTcBK * 2];  // gate weight: 16 KB per stage, 1024-byte aligned
+  uint8_t b[kTcStages][BNT * kTcBK * 2];    // tokens: BNT * 128 bytes per stage
   uint64_t full[kTcStages];
   uint64_t empty[kTcStages];
   uint64_t tmem_full;
+  uint64_t rx_full;  // split-K: the peers' partials of this CTA's tokens have landed
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -108,6 +115,36 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Bulk copy of `bytes` from this CTA's shared memory into a peer's, completing
+// on the peer's mbarrier (both peer addresses from mapa).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(src), "r"(bytes), "r"(bar_cluster)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+// Store logits[t, e .. e + 3] (the columns below E), as one 16-byte store
+// when `vec` (E a multiple of 4 and a 16-byte aligned base).
+__device__ __forceinline__ void store4(float* __restrict__ logits, int t, int e, int E, bool vec, float4 v) {
+  float* dst = logits + static_cast<int64_t>(t) * E + e;
+  if (vec) {
+    if (e < E) *reinterpret_cast<float4*>(dst) = v;
+  } else {
+    if (e < E) dst[0] = v.x;
+    if (e + 1 < E) dst[1] = v.y;
+    if (e + 2 < E) dst[2] = v.z;
+    if (e + 3 < E) dst[3] = v.w;
+  }
+}
+
 __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -123,45 +160,38 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]
 
 // Bounded wait; gives up early once the CTA's abort flag is raised unless
 // `drain` is set (a drain must see the phase, abort or not).
+// The try_wait carries no suspend-time hint: with a 1 us hint the waits on
+// the stage ring added 1.4 us to a 128-CTA launch at T = 8192.
+__device__ __forceinline__ bool tc_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, bool drain) {
   for (int it = 0; it < kTcMaxWaits; ++it) {
-    if (mbar_try_wait(bar, parity, kTcHintNs)) return true;
+    if (tc_try_wait(bar, parity)) return true;
     if (!drain && *abort_flag) return false;
   }
   *abort_flag = 1;
   return false;
 }
 
-// Store 32 consecutive FP32 values of one row (the first `nvalid`), as 16-byte
-// vectors when the row slice is aligned; NaN when the pipeline gave up.
-__device__ __forceinline__ void store_row32(float* dst, const uint32_t (&v)[32], int nvalid, bool ok) {
-  const float nan = __int_as_float(0x7FC00000);
-  if (nvalid == 32 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-#pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-      float4 f;
-      f.x = ok ? __uint_as_float(v[i]) : nan;
-      f.y = ok ? __uint_as_float(v[i + 1]) : nan;
-      f.z = ok ? __uint_as_float(v[i + 2]) : nan;
-      f.w = ok ? __uint_as_float(v[i + 3]) : nan;
-      *reinterpret_cast<float4*>(dst + i) = f;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < nvalid) dst[i] = ok ? __uint_as_float(v[i]) : nan;
-  }
-}
-
-template <int BN>
+template <int BNT>
 __global__ void __launch_bounds__(kTcThreads, 1)
 router_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                  float* __restrict__ logits, int T, int H, int E) {
   extern __shared__ uint8_t smem_raw[];
-  TcSmem<BN>& sm = *reinterpret_cast<TcSmem<BN>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                  ~static_cast<uintptr_t>(1023));
+  TcSmem<BNT>& sm = *reinterpret_cast<TcSmem<BNT>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                    ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * kTcBM, n0 = blockIdx.y * BN;
+  const int t0 = blockIdx.x * BNT, e0 = blockIdx.y * kTcBM;
   const int S = gridDim.z;  // split-K: the cluster's CTAs take consecutive K ranges
   const int nkb_all = (H + kTcBK - 1) / kTcBK;
   const int kb0 = static_cast<int>(static_cast<int64_t>(nkb_all) * blockIdx.z / S);
@@ -174,10 +204,11 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
       mbar_init(&sm.empty[s], 1);
     }
     mbar_init(&sm.tmem_full, 1);
+    mbar_init(&sm.rx_full, 1);
     sm.abort_flag = 0;
     mbar_init_fence();
   }
-  if (warp == 1) tmem_alloc(&sm.tmem_base, BN);
+  if (warp == 1) tmem_alloc(&sm.tmem_base, BNT);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -193,9 +224,9 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = kb % kTcStages, n = kb / kTcStages;
         if (n > 0 && !tc_wait(&sm.empty[s], (n - 1) & 1, abort_v, false)) break;
-        mbar_arrive_expect_tx(&sm.full[s], static_cast<uint32_t>((kTcBM + BN) * kTcBK * 2));
-        tma_load_2d(sm.a[s], &tmap_x, (kb0 + kb) * kTcBK, m0, &sm.full[s]);
-        tma_load_2d(sm.b[s], &tmap_w, (kb0 + kb) * kTcBK, n0, &sm.full[s]);
+        mbar_arrive_expect_tx(&sm.full[s], static_cast<uint32_t>((kTcBM + BNT) * kTcBK * 2));
+        tma_load_2d(sm.a[s], &tmap_w, (kb0 + kb) * kTcBK, e0, &sm.full[s]);
+        tma_load_2d(sm.b[s], &tmap_x, (kb0 + kb) * kTcBK, t0, &sm.full[s]);
         issued = kb + 1;
       }
       // drain: no copy may land after this CTA exits
@@ -205,7 +236,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc_bf16(kTcBM, BN);
+      constexpr uint32_t idesc = umma_idesc_bf16(kTcBM, BNT);
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = kb % kTcStages, n = kb / kTcStages;
         if (!tc_wait(&sm.full[s], n & 1, abort_v, false)) break;
@@ -223,74 +254,90 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
     __syncwarp();
   }
   // ------------------------------------------------------------------ epilogue
-  // Warps 2..5 own tensor-memory lane quarter q = warp % 4 (32 tokens each).
-  // Without split-K they store their rows.  With split-K every CTA of the
-  // cluster pushes its partial rows into the shared memory of the CTA that
-  // owns them (rows [r * 128/S, (r+1) * 128/S) belong to rank r; the stage
-  // ring is free by then), and each owner adds the S partials in rank order.
+  // Warps 2..5 own tensor-memory lane quarter q = warp % 4: experts
+  // e0 + 32 q + lane.  Each CTA first writes its accumulator as a [token]
+  // [expert] tile into its own token ring.  Without split-K the tile is stored
+  // as it is.  With split-K tokens [r * BNT/S, (r+1) * BNT/S) of the tile
+  // belong to rank r: every CTA sends each peer that peer's rows with one bulk
+  // copy into the peer's (idle) weight ring, and each owner adds the S
+  // partials in rank order (deterministic) and stores the sums.
+  static_assert(BNT * kTcBM * 4 <= sizeof(sm.a) && BNT * kTcBM * 4 <= sizeof(sm.b),
+                "the partial tile must fit in either operand ring");
   __syncwarp();  // warps 0 and 1 reconverge after their lane-0 loops
   const bool epi = warp >= 2;
   const int q = warp & 3;
-  const int row_t = q * 32 + lane;  // row of the tile
+  const int e_t = q * 32 + lane;  // expert within the tile
+  const int etid = threadIdx.x - 64;  // 0..127 in the epilogue warps
+  float* part = reinterpret_cast<float*>(&sm.b[0][0]);  // [BNT][kTcBM]
+  const bool vec = (E & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
+  const float nan = __int_as_float(0x7FC00000);
   bool ok = true;
   if (epi) {
     ok = tc_wait(&sm.tmem_full, 0, abort_v, true) && !*abort_v;
     tc_fence_after_sync();
+#pragma unroll 1
+    for (int c = 0; c < BNT; c += 32) {
+      uint32_t v[32];
+      tmem_ld_32cols(tmem_d + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c), v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) part[(c + i) * kTcBM + e_t] = ok ? __uint_as_float(v[i]) : nan;
+    }
   }
-  constexpr int PITCH = BN + 4;  // floats per received row (padding spreads the banks)
+  // The 128 epilogue threads store 4 experts each, 4 token rows per pass.
+  const int c4 = (etid & 31) * 4;
   if (S == 1) {
     if (epi) {
-      const int row = m0 + row_t;
-#pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t v[32];
-        tmem_ld_32cols(tmem_d + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c), v);
-        if (row < T) store_row32(logits + static_cast<int64_t>(row) * E + n0 + c, v, min(32, E - (n0 + c)), ok);
-      }
+      named_barrier(1, 128);
+#pragma unroll 4
+      for (int r = etid >> 5; r < BNT && t0 + r < T; r += 4)
+        store4(logits, t0 + r, e0 + c4, E, vec, *reinterpret_cast<const float4*>(part + r * kTcBM + c4));
     }
   } else {
-    cg::cluster_group cluster = cg::this_cluster();
-    const int rpo = kTcBM / S;                 // rows owned per rank
-    float* recv = reinterpret_cast<float*>(&sm.a[0][0]);  // [S][rpo][PITCH]
-    cluster_arrive_release();                  // every CTA's MMAs are done; stage rings are free
+    const int rpo = BNT / S;  // tokens owned per rank
+    const int rank = static_cast<int>(cg::this_cluster().block_rank());
+    const uint32_t chunk = static_cast<uint32_t>(rpo * kTcBM * 4);
+    float* recv = reinterpret_cast<float*>(&sm.a[0][0]);  // [S][rpo][kTcBM]
+    if (threadIdx.x == 64) mbar_arrive_expect_tx(&sm.rx_full, static_cast<uint32_t>(S - 1) * chunk);
+    if (epi) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tile is read by bulk copies
+    cluster_arrive_release();  // every CTA's MMAs are done (rings free) and its tile written
     cluster_wait_acquire();
-    if (epi) {
-      const int owner = row_t / rpo, rl = row_t - owner * rpo;
-      float* dst = cluster.map_shared_rank(recv, owner) +
-                   (static_cast<int>(cluster.block_rank()) * rpo + rl) * PITCH;
-#pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t v[32];
-        tmem_ld_32cols(tmem_d + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c), v);
-        const float nan = __int_as_float(0x7FC00000);
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(dst + c + i) =
-              ok ? make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
-                               __uint_as_float(v[i + 3]))
-                 : make_float4(nan, nan, nan, nan);
+    if (threadIdx.x == 64) {
+      for (int o = 0; o < S; ++o) {
+        if (o == rank) continue;
+        bulk_copy_to_peer(peer_addr(smem_addr(recv) + static_cast<uint32_t>(rank) * chunk, o),
+                          smem_addr(part) + static_cast<uint32_t>(o) * chunk, chunk, peer_addr(smem_addr(&sm.rx_full), o));
       }
     }
+    if (epi) ok = tc_wait(&sm.rx_full, 0, abort_v, true) && ok;
+    // Arrive once this CTA holds every partial of its tokens; no CTA leaves
+    // before all have arrived, so no copy reads the memory of a CTA that exited.
     cluster_arrive_release();
-    cluster_wait_acquire();
     if (epi) {
-      const int me = static_cast<int>(cluster.block_rank());
-      const int et = threadIdx.x - 64;  // 0..127
-      for (int e = et; e < rpo * BN; e += 128) {
-        const int rl = e / BN, col = e - rl * BN;
-        float acc = 0.f;
-        for (int r = 0; r < S; ++r) acc += recv[(r * rpo + rl) * PITCH + col];
-        const int row = m0 + me * rpo + rl;
-        if (row < T && n0 + col < E)
-          logits[static_cast<int64_t>(row) * E + n0 + col] = ok ? acc : __int_as_float(0x7FC00000);  // a peer's NaN propagates
+      // sum in rank order (a peer's NaN propagates), then store
+      for (int r = etid >> 5; r < rpo && t0 + rank * rpo + r < T; r += 4) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (j < S) {
+            const float* src = j == rank ? part + (rank * rpo + r) * kTcBM : recv + (j * rpo + r) * kTcBM;
+            const float4 p = *reinterpret_cast<const float4*>(src + c4);
+            acc.x += p.x;
+            acc.y += p.y;
+            acc.z += p.z;
+            acc.w += p.w;
+          }
+        }
+        if (!ok) acc = make_float4(nan, nan, nan, nan);
+        store4(logits, t0 + rank * rpo + r, e0 + c4, E, vec, acc);
       }
     }
+    cluster_wait_acquire();
   }
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_d, BN);
+    tmem_dealloc(tmem_d, BNT);
   }
 }
 
@@ -324,21 +371,21 @@ static bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t c
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN>
+template <int BNT>
 static cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw, float* logits, int T, int H, int E,
                              int S, cudaStream_t stream) {
-  const size_t smem = sizeof(TcSmem<BN>) + 1024;
+  const size_t smem = sizeof(TcSmem<BNT>) + 1024;
   static bool opt_in[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
   if (dev >= 0 && dev < 64 && !opt_in[dev]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(router_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    const cudaError_t e = cudaFuncSetAttribute(router_tc_kernel<BNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     opt_in[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((T + kTcBM - 1) / kTcBM, (E + BN - 1) / BN, S);
+  cfg.gridDim = dim3((T + BNT - 1) / BNT, (E + kTcBM - 1) / kTcBM, S);
   cfg.blockDim = dim3(kTcThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -353,27 +400,25 @@ static cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw, float
     cfg.numAttrs = 2;
   }
   cfg.attrs = attr;
-  return cudaLaunchKernelEx(&cfg, router_tc_kernel<BN>, mx, mw, logits, T, H, E);
+  return cudaLaunchKernelEx(&cfg, router_tc_kernel<BNT>, mx, mw, logits, T, H, E);
 }
 
 cudaError_t launch_router_tc(const void* x, const void* w, float* logits, int T, int H, int E, int nsm,
                              cudaStream_t stream) {
-  // 128 expert columns per tile (64 for E <= 64); then split K over a cluster of
-  // S CTAs until the grid covers about three quarters of the SMs: a CTA's time
-  // is set by its K blocks, since each SM streams at its own latency-bound
-  // rate.  S = 8 only while the grid stays within 64 CTAs: sixteen clusters of
-  // 8 CTAs of ~200 KB shared memory did not all fit in one wave (T = 1024:
-  // 24 us with S = 8 against 13 us for eight such clusters at T = 512).
-  const int mt = (T + kTcBM - 1) / kTcBM;
-  const int bn = E > 64 ? 128 : 64;
-  const int tiles = mt * ((E + bn - 1) / bn);
+  // 128-expert x 128-token tiles (an expert count below 128 runs on zero-filled
+  // weight rows); then split K over a cluster of S CTAs until the grid covers
+  // about three quarters of the SMs: a CTA's time is set by its K blocks,
+  // since each SM streams at its own latency-bound rate.  S = 8 only while the
+  // grid stays within 64 CTAs: sixteen clusters of 8 CTAs of ~200 KB shared
+  // memory did not all fit in one wave (T = 1024: 24 us with S = 8 against
+  // 13 us for eight such clusters at T = 512).
+  const int tiles = ((T + kTcBNT - 1) / kTcBNT) * ((E + kTcBM - 1) / kTcBM);
   const int nkb = (H + kTcBK - 1) / kTcBK;
   int S = 1;
   while (S < 8 && tiles * S < nsm * 3 / 4 && nkb >= 2 * S * 2 && (S < 4 || tiles * 2 * S <= 64)) S *= 2;
   CUtensorMap mx, mw;
-  if (!make_map(&mx, x, T, H, kTcBM) || !make_map(&mw, w, E, H, bn)) return cudaErrorInvalidValue;
-  return bn == 128 ? launch_tc<128>(mx, mw, logits, T, H, E, S, stream)
-                   : launch_tc<64>(mx, mw, logits, T, H, E, S, stream);
+  if (!make_map(&mx, x, T, H, kTcBNT) || !make_map(&mw, w, E, H, kTcBM)) return cudaErrorInvalidValue;
+  return launch_tc<kTcBNT>(mx, mw, logits, T, H, E, S, stream);
 }
 
 bool router_tc_supported(int64_t T, int64_t H) { return T >= kRouterTcMinT && H >= kTcBK; }
