@@ -4,11 +4,12 @@
 // BF16 GEMM).  At T in the thousands the router is a dense contraction near
 // the tensor-core ridge, so it is tiled for tcgen05:
 //  - one CTA per 128-expert x BNT-token tile: the gate weight is the M side
-//    (UMMA M = 128) and the tokens the N side (N = BNT), so tensor-memory lane
-//    i holds expert i of the tile and column j token j;
+//    (UMMA M = 128) and the tokens the N side (N = BNT, 64..128 in steps of
+//    16, chosen per launch so that the grid fills the SMs), so tensor-memory
+//    lane i holds expert i of the tile and column j token j;
 //  - warp 0 streams 64-wide K blocks of both operands with TMA (128-byte
 //    swizzle, out-of-range rows and columns zero-filled) into a 6-stage ring;
-//  - warp 1 allocates BNT tensor-memory columns and one lane issues
+//  - warp 1 allocates tensor-memory columns for BNT and one lane issues
 //    tcgen05.mma (kind::f16, 4 per K block), releasing each stage with
 //    tcgen05.commit when the MMAs that read it complete;
 //  - warps 2..5 wait for the final commit and read the accumulator with
@@ -22,6 +23,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "host_util.h"
 #include "router_tc.h"
@@ -29,11 +32,13 @@
 namespace moe {
 
 constexpr int kTcBM = 128;       // experts per tile (UMMA M)
-constexpr int kTcBNT = 128;      // tokens per tile (UMMA N)
 constexpr int kTcBK = 64;        // K elements per stage: one 128-byte swizzle row
 constexpr int kTcStages = 6;
 constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
 constexpr int kTcMaxWaits = 1 << 21;
+
+// Tensor-memory columns for an N-wide accumulator: a power of two >= 32.
+__host__ __device__ constexpr uint32_t tmem_cols(int n) { return n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : 256u; }
 
 template <int BNT>
 struct TcSmem {
@@ -208,7 +213,8 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
     sm.abort_flag = 0;
     mbar_init_fence();
   }
-  if (warp == 1) tmem_alloc(&sm.tmem_base, BNT);
+  static_assert(BNT % 16 == 0 && BNT >= 16 && BNT <= 128, "UMMA N for M = 128");
+  if (warp == 1) tmem_alloc(&sm.tmem_base, tmem_cols(BNT));
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -280,7 +286,8 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
       uint32_t v[32];
       tmem_ld_32cols(tmem_d + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c), v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) part[(c + i) * kTcBM + e_t] = ok ? __uint_as_float(v[i]) : nan;
+      for (int i = 0; i < 32; ++i)
+        if (c + i < BNT) part[(c + i) * kTcBM + e_t] = ok ? __uint_as_float(v[i]) : nan;
     }
   }
   // The 128 epilogue threads store 4 experts each, 4 token rows per pass.
@@ -337,7 +344,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_d, BNT);
+    tmem_dealloc(tmem_d, tmem_cols(BNT));
   }
 }
 
@@ -372,22 +379,64 @@ static bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t c
 }
 
 template <int BNT>
-static cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw, float* logits, int T, int H, int E,
-                             int S, cudaStream_t stream) {
-  const size_t smem = sizeof(TcSmem<BNT>) + 1024;
-  static bool opt_in[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  if (dev >= 0 && dev < 64 && !opt_in[dev]) {
+static size_t tc_smem_bytes() {
+  return sizeof(TcSmem<BNT>) + 1024;  // + alignment slack for the 1024-byte swizzle atoms
+}
+
+// Opt the kernel into its dynamic shared memory, once per device.
+template <int BNT>
+static cudaError_t tc_opt_in(int dev) {
+  static std::atomic<bool> done[64];
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!done[dev].load()) {
     const cudaError_t e = cudaFuncSetAttribute(router_tc_kernel<BNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(smem));
+                                               static_cast<int>(tc_smem_bytes<BNT>()));
     if (e != cudaSuccess) return e;
-    opt_in[dev] = true;
+    done[dev].store(true);
   }
+  return cudaSuccess;
+}
+
+// How many clusters of S CTAs (S = 2, 4, 8) of this kernel the device holds
+// at once (cudaOccupancyMaxActiveClusters, cached per device); 0 if unknown.
+template <int BNT>
+static int tc_max_clusters(int dev, int S) {
+  static std::atomic<int> cache[64][3];  // 0 = not asked yet, else count + 1
+  const int si = S == 2 ? 0 : S == 4 ? 1 : 2;
+  if (dev < 0 || dev >= 64 || tc_opt_in<BNT>(dev) != cudaSuccess) return 0;
+  int c = cache[dev][si].load();
+  if (c == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, S);
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = tc_smem_bytes<BNT>();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = S;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, router_tc_kernel<BNT>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    c = n + 1;
+    cache[dev][si].store(c);
+  }
+  return c - 1;
+}
+
+template <int BNT>
+static cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw, float* logits, int T, int H, int E,
+                             int S, int dev, cudaStream_t stream) {
+  const cudaError_t oe = tc_opt_in<BNT>(dev);
+  if (oe != cudaSuccess) return oe;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((T + BNT - 1) / BNT, (E + kTcBM - 1) / kTcBM, S);
   cfg.blockDim = dim3(kTcThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = tc_smem_bytes<BNT>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0] = pdl_attribute();
@@ -403,22 +452,71 @@ static cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw, float
   return cudaLaunchKernelEx(&cfg, router_tc_kernel<BNT>, mx, mw, logits, T, H, E);
 }
 
+static int max_clusters_for(int bnt, int dev, int S) {
+  switch (bnt) {
+    case 64: return tc_max_clusters<64>(dev, S);
+    case 80: return tc_max_clusters<80>(dev, S);
+    case 96: return tc_max_clusters<96>(dev, S);
+    case 112: return tc_max_clusters<112>(dev, S);
+    default: return tc_max_clusters<128>(dev, S);
+  }
+}
+
+// Launch shape of one router call: token tile and split-K factor.
+struct TcShape {
+  int bnt, S;
+};
+
+// Choose the token tile BNT (64..128, steps of 16) and the split-K cluster
+// size S (1, 2, 4, 8) by a small cost model: a CTA's time is its K blocks'
+// bytes at the rate one SM streams them (about 120 GB/s, latency-bound), plus
+// about 3 us for the split-K exchange, times the number of waves.  Split-K
+// grids must fit in one wave of clusters as the device reports it (on GB300
+// with ~200 KB of shared memory per CTA: 76 clusters of 2, 36 of 4, 15 of 8;
+// sixteen clusters of 8 took two waves, 24 against 13 us), and every rank
+// keeps >= 2 K blocks.  Ties go to the larger tile.
+static TcShape choose_shape(int T, int H, int E, int nsm, int dev) {
+  const int nkb = (H + kTcBK - 1) / kTcBK;
+  const int ne = (E + kTcBM - 1) / kTcBM;
+  TcShape best{128, 1};
+  double best_us = 1e30;
+  for (int bnt = 128; bnt >= 64; bnt -= 16) {
+    const int tiles = ((T + bnt - 1) / bnt) * ne;
+    for (int S = 1; S <= 8; S *= 2) {
+      const int ctas = tiles * S;
+      if (S > 1 && (nkb < 2 * S || ctas > nsm || tiles > max_clusters_for(bnt, dev, S))) continue;
+      const int waves = (ctas + nsm - 1) / nsm;
+      const double bytes = static_cast<double>((nkb + S - 1) / S) * (kTcBM + bnt) * kTcBK * 2;
+      const double us = waves * (bytes / 120e3 + (S > 1 ? 3.0 : 0.0));
+      if (us < best_us * 0.999) {
+        best_us = us;
+        best = TcShape{bnt, S};
+      }
+    }
+  }
+  return best;
+}
+
+template <int BNT>
+static cudaError_t launch_bnt(const void* x, const void* w, float* logits, int T, int H, int E, int S, int dev,
+                              cudaStream_t stream) {
+  CUtensorMap mx, mw;
+  if (!make_map(&mx, x, T, H, BNT) || !make_map(&mw, w, E, H, kTcBM)) return cudaErrorInvalidValue;
+  return launch_tc<BNT>(mx, mw, logits, T, H, E, S, dev, stream);
+}
+
 cudaError_t launch_router_tc(const void* x, const void* w, float* logits, int T, int H, int E, int nsm,
                              cudaStream_t stream) {
-  // 128-expert x 128-token tiles (an expert count below 128 runs on zero-filled
-  // weight rows); then split K over a cluster of S CTAs until the grid covers
-  // about three quarters of the SMs: a CTA's time is set by its K blocks,
-  // since each SM streams at its own latency-bound rate.  S = 8 only while the
-  // grid stays within 64 CTAs: sixteen clusters of 8 CTAs of ~200 KB shared
-  // memory did not all fit in one wave (T = 1024: 24 us with S = 8 against
-  // 13 us for eight such clusters at T = 512).
-  const int tiles = ((T + kTcBNT - 1) / kTcBNT) * ((E + kTcBM - 1) / kTcBM);
-  const int nkb = (H + kTcBK - 1) / kTcBK;
-  int S = 1;
-  while (S < 8 && tiles * S < nsm * 3 / 4 && nkb >= 2 * S * 2 && (S < 4 || tiles * 2 * S <= 64)) S *= 2;
-  CUtensorMap mx, mw;
-  if (!make_map(&mx, x, T, H, kTcBNT) || !make_map(&mw, w, E, H, kTcBM)) return cudaErrorInvalidValue;
-  return launch_tc<kTcBNT>(mx, mw, logits, T, H, E, S, stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  const TcShape sh = choose_shape(T, H, E, nsm, dev);
+  switch (sh.bnt) {
+    case 64: return launch_bnt<64>(x, w, logits, T, H, E, sh.S, dev, stream);
+    case 80: return launch_bnt<80>(x, w, logits, T, H, E, sh.S, dev, stream);
+    case 96: return launch_bnt<96>(x, w, logits, T, H, E, sh.S, dev, stream);
+    case 112: return launch_bnt<112>(x, w, logits, T, H, E, sh.S, dev, stream);
+    default: return launch_bnt<128>(x, w, logits, T, H, E, sh.S, dev, stream);
+  }
 }
 
 bool router_tc_supported(int64_t T, int64_t H) { return T >= kRouterTcMinT && H >= kTcBK; }
