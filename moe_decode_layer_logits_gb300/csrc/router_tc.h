@@ -6,9 +6,12 @@
 
 namespace moe {
 
-// Batches of at least this many tokens (with H >= 64) take the tcgen05 kernel
-// (measured at H = 6144, E = 256: 11.4 against 19.8 us at T = 256).
-constexpr int64_t kRouterTcMinT = 256;
+// Batches of more than 64 tokens (with H >= 64) take the tcgen05 kernel
+// (measured at H = 6144, E = 256: T = 96 / 128 / 224 in 8.5 / 8.4 / 8.7 us
+// against 10.4 / 10.3 / 10.7 us for the register-fed mma.sync kernel with
+// 32-token tiles and 9.5 / 9.9 / 14.2 us with 16-token tiles; at T = 64 the
+// mma.sync kernel takes 4.8 against 8.3 us).
+constexpr int64_t kRouterTcMinT = 65;
 
 bool router_tc_supported(int64_t T, int64_t H);
 

@@ -50,15 +50,15 @@ def bits(t):
 
 ROUTER = [  # (T, H, E)
     (4, 2048, 64), (1, 6144, 256), (4, 6144, 256), (64, 6144, 256), (12, 6144, 256), (28, 2048, 256),
-    (37, 2056, 72), (200, 6144, 256), (5, 512, 20), (3, 64, 1), (9, 1024, 1024), (16, 8, 16), (130, 6144, 168),
-    # from 256 tokens the tcgen05 kernel: full and partial token tiles of each
+    (37, 2056, 72), (5, 512, 20), (3, 64, 1), (9, 1024, 1024), (16, 8, 16), (100, 48, 40),
+    # from 65 tokens (H >= 64) the tcgen05 kernel: full and partial token tiles of each
     # width it picks (64, 80, 96, 112, 128 tokens), partial 64-wide K blocks
     # (H = 2056), partial expert tiles (E = 168, 72, 1) and split-K clusters of
     # 1, 2, 4 and 8 CTAs
     (1024, 6144, 256), (1500, 2056, 168), (1100, 512, 72), (1024, 64, 1), (1280, 1024, 1024),
     (256, 6144, 256), (300, 2048, 64), (513, 6144, 256), (8192, 512, 256),
     (384, 6144, 256), (512, 6144, 256), (768, 6144, 256), (2000, 6144, 168), (2048, 6144, 256),
-    (4000, 6144, 256),
+    (4000, 6144, 256), (65, 6144, 256), (130, 6144, 168), (200, 6144, 256),
 ]
 
 
