@@ -170,6 +170,19 @@ int moe_tail_fused(const float* logits, int64_t E, int32_t k, float routed_scale
  */
 int moe_debug_withhold_stream_stage(int32_t stage);
 
+/*
+ * Test hook of the launch-shape choice of the tensor-memory router (batches
+ * of more than 64 tokens); no counterpart on the pages.  Host only, launches
+ * nothing.  For a device with `nsm` SMs that holds mc2 / mc4 / mc8 clusters
+ * of 2 / 4 / 8 router CTAs at once, writes the token tile the router would
+ * take (64, 80, 96, 112 or 128 tokens per CTA, 128 experts each) to *bnt
+ * and its split-K cluster size (1, 2, 4 or 8) to *split_k.  Returns MOE_OK,
+ * or MOE_ERR_INVALID_ARG for T outside [1, 2^30], H outside [64, 2^20], E outside [1, MOE_MAX_E],
+ * nsm < 1, a negative cluster count or a NULL output.
+ */
+int moe_debug_router_tc_shape(int64_t T, int64_t H, int64_t E, int32_t nsm, int32_t mc2, int32_t mc4,
+                              int32_t mc8, int32_t* bnt, int32_t* split_k);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,6 +14,8 @@ allocated with torch when not given.
 
 from __future__ import annotations
 
+import ctypes
+
 import torch
 
 from . import _lib
@@ -21,6 +23,7 @@ from ._lib import MoeTailError, check, lib
 
 __all__ = [
     "moe_debug_withhold_stream_stage",
+    "moe_debug_router_tc_shape",
     "moe_router_logits_fp32",
     "moe_topk_route",
     "moe_finalize_add_rmsnorm",
@@ -137,3 +140,13 @@ def moe_debug_withhold_stream_stage(stage):
     leaves stage `stage` of its first CTA uncopied, so that CTA's wait runs
     out and MOE_FLAG_TIMEOUT is set; -1 cancels the request."""
     check(lib().moe_debug_withhold_stream_stage(int(stage)), "moe_debug_withhold_stream_stage")
+
+
+def moe_debug_router_tc_shape(T, H, E, nsm, mc2, mc4, mc8):
+    """Test hook (host only): the (token tile, split-K cluster size) the
+    tensor-memory router would take for T x H x E on a device with `nsm` SMs
+    that holds mc2 / mc4 / mc8 clusters of 2 / 4 / 8 router CTAs at once."""
+    bnt, split_k = ctypes.c_int32(), ctypes.c_int32()
+    check(lib().moe_debug_router_tc_shape(int(T), int(H), int(E), int(nsm), int(mc2), int(mc4), int(mc8),
+                                          ctypes.byref(bnt), ctypes.byref(split_k)), "moe_debug_router_tc_shape")
+    return bnt.value, split_k.value

@@ -475,7 +475,9 @@ struct TcShape {
 // with ~200 KB of shared memory per CTA: 76 clusters of 2, 36 of 4, 15 of 8;
 // sixteen clusters of 8 took two waves, 24 against 13 us), and every rank
 // keeps >= 2 K blocks.  Ties go to the larger tile.
-static TcShape choose_shape(int T, int H, int E, int nsm, int dev) {
+// `max_clusters(bnt, S)` gives how many clusters of S CTAs fit at once.
+template <class MaxClusters>
+static TcShape choose_shape(int T, int H, int E, int nsm, MaxClusters max_clusters) {
   const int nkb = (H + kTcBK - 1) / kTcBK;
   const int ne = (E + kTcBM - 1) / kTcBM;
   TcShape best{128, 1};
@@ -484,7 +486,7 @@ static TcShape choose_shape(int T, int H, int E, int nsm, int dev) {
     const int tiles = ((T + bnt - 1) / bnt) * ne;
     for (int S = 1; S <= 8; S *= 2) {
       const int ctas = tiles * S;
-      if (S > 1 && (nkb < 2 * S || ctas > nsm || tiles > max_clusters_for(bnt, dev, S))) continue;
+      if (S > 1 && (nkb < 2 * S || ctas > nsm || tiles > max_clusters(bnt, S))) continue;
       const int waves = (ctas + nsm - 1) / nsm;
       const double bytes = static_cast<double>((nkb + S - 1) / S) * (kTcBM + bnt) * kTcBK * 2;
       const double us = waves * (bytes / 120e3 + (S > 1 ? 3.0 : 0.0));
@@ -509,7 +511,7 @@ cudaError_t launch_router_tc(const void* x, const void* w, float* logits, int T,
                              cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  const TcShape sh = choose_shape(T, H, E, nsm, dev);
+  const TcShape sh = choose_shape(T, H, E, nsm, [dev](int bnt, int S) { return max_clusters_for(bnt, dev, S); });
   switch (sh.bnt) {
     case 64: return launch_bnt<64>(x, w, logits, T, H, E, sh.S, dev, stream);
     case 80: return launch_bnt<80>(x, w, logits, T, H, E, sh.S, dev, stream);
@@ -522,3 +524,18 @@ cudaError_t launch_router_tc(const void* x, const void* w, float* logits, int T,
 bool router_tc_supported(int64_t T, int64_t H) { return T >= kRouterTcMinT && H >= kTcBK; }
 
 }  // namespace moe
+
+// Host-only test hook: the launch shape the tcgen05 router would take for a
+// device with `nsm` SMs that holds mc2 / mc4 / mc8 clusters of 2 / 4 / 8 CTAs
+// at once (for every token tile).
+extern "C" int moe_debug_router_tc_shape(int64_t T, int64_t H, int64_t E, int32_t nsm, int32_t mc2, int32_t mc4,
+                                         int32_t mc8, int32_t* bnt, int32_t* split_k) {
+  if (T < 1 || T > (int64_t{1} << 30) || H < moe::kTcBK || H > (1 << 20) || E < 1 || E > MOE_MAX_E || nsm < 1 ||
+      mc2 < 0 || mc4 < 0 || mc8 < 0 || !bnt || !split_k)
+    return MOE_ERR_INVALID_ARG;
+  const moe::TcShape sh = moe::choose_shape(static_cast<int>(T), static_cast<int>(H), static_cast<int>(E), nsm,
+                                            [=](int, int S) { return S == 2 ? mc2 : S == 4 ? mc4 : mc8; });
+  *bnt = sh.bnt;
+  *split_k = sh.S;
+  return MOE_OK;
+}

@@ -204,3 +204,74 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(L, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         L.lib()
+
+
+# ---------------------------------------------------------------------------
+# launch shape of the tensor-memory router (host logic, no launch)
+# ---------------------------------------------------------------------------
+
+# clusters of 2 / 4 / 8 router CTAs one GB300 (152 SMs) holds at once, as
+# cudaOccupancyMaxActiveClusters reports them for ~200 KB of shared memory
+GB300_SMS, GB300_CLUSTERS = 152, (76, 36, 15)
+
+
+def _shape(T, H, E, nsm=GB300_SMS, mc=GB300_CLUSTERS):
+    import moe_decode_layer_logits_gb300 as M
+    return M.moe_debug_router_tc_shape(T, H, E, nsm, *mc)
+
+
+def _modelled_us(T, H, E, nsm, bnt, S):
+    # the cost model the choice is documented to minimise: a CTA's K-block
+    # bytes at ~120 GB/s per SM, ~3 us per split-K exchange, times the waves
+    nkb = -(-H // 64)
+    ctas = -(-T // bnt) * -(-E // 128) * S
+    waves = -(-ctas // nsm)
+    return waves * (-(-nkb // S) * (128 + bnt) * 128 / 120e3 + (3.0 if S > 1 else 0.0))
+
+
+def _feasible(T, H, E, nsm, mc, bnt, S):
+    if S == 1:
+        return True
+    tiles = -(-T // bnt) * -(-E // 128)
+    nkb = -(-H // 64)
+    return nkb >= 2 * S and tiles * S <= nsm and tiles <= mc[{2: 0, 4: 1, 8: 2}[S]]
+
+
+def test_router_tc_shape_at_the_measured_sizes(lib):
+    # H = 6144, E = 256: the shapes behind the timings in the design notes
+    want = {256: (64, 8), 512: (80, 8), 1024: (64, 4), 2048: (128, 4), 4096: (112, 2), 8192: (112, 1)}
+    for T, shape in want.items():
+        assert _shape(T, 6144, 256) == shape, T
+
+
+def test_router_tc_shape_is_feasible_and_minimal(lib):
+    devices = [(GB300_SMS, GB300_CLUSTERS), (132, (66, 30, 14)), (20, (10, 4, 2)), (GB300_SMS, (0, 0, 0))]
+    for T in [65, 100, 128, 255, 256, 300, 513, 777, 1024, 1500, 2048, 3000, 4096, 8192, 16384, 100000]:
+        for H in [64, 512, 2056, 6144]:
+            for E in [1, 72, 168, 256, 1024]:
+                for nsm, mc in devices:
+                    bnt, S = _shape(T, H, E, nsm, mc)
+                    assert bnt in (64, 80, 96, 112, 128) and S in (1, 2, 4, 8)
+                    assert bnt % S == 0  # every rank owns whole token rows
+                    assert _feasible(T, H, E, nsm, mc, bnt, S), (T, H, E, nsm, bnt, S)
+                    best = min(_modelled_us(T, H, E, nsm, b, s)
+                               for b in (64, 80, 96, 112, 128) for s in (1, 2, 4, 8)
+                               if _feasible(T, H, E, nsm, mc, b, s))
+                    assert _modelled_us(T, H, E, nsm, bnt, S) <= best * 1.001, (T, H, E, nsm, bnt, S)
+                    if mc == (0, 0, 0):
+                        assert S == 1  # no cluster fits: no split-K
+
+
+def test_router_tc_shape_argument_checks(lib):
+    import ctypes
+    b, s = ctypes.c_int32(), ctypes.c_int32()
+    ok = dict(T=512, H=6144, E=256, nsm=152, mc2=76, mc4=36, mc8=15)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return lib.moe_debug_router_tc_shape(a["T"], a["H"], a["E"], a["nsm"], a["mc2"], a["mc4"], a["mc8"],
+                                             kw.get("pb", ctypes.byref(b)), kw.get("ps", ctypes.byref(s)))
+    assert call() == L.MOE_OK
+    for bad in [dict(T=0), dict(H=32), dict(E=0), dict(E=1025), dict(nsm=0), dict(mc4=-1), dict(pb=None),
+                dict(ps=None)]:
+        assert call(**bad) == L.MOE_ERR_INVALID_ARG, bad
