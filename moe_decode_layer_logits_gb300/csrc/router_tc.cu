@@ -1,8 +1,10 @@
-// Router GEMM for prefill-size batches on the 5th-generation tensor cores:
-// logits[T, E] = x[T, H] . W[E, H]^T, BF16 operands, FP32 accumulation in
-// tensor memory (lmdeploy pull 4853, Summary: FP32 router logits through a
+// Router GEMM for batches of more than 64 tokens on the 5th-generation tensor
+// cores: logits[T, E] = x[T, H] . W[E, H]^T, BF16 operands, FP32 accumulation
+// in tensor memory (lmdeploy pull 4853, Summary: FP32 router logits through a
 // BF16 GEMM).  At T in the thousands the router is a dense contraction near
-// the tensor-core ridge, so it is tiled for tcgen05:
+// the tensor-core ridge, and from about a hundred tokens up the deep per-SM
+// copy stream below already beats register-fed MMAs, so it is tiled for
+// tcgen05:
 //  - one CTA per 128-expert x BNT-token tile: the gate weight is the M side
 //    (UMMA M = 128) and the tokens the N side (N = BNT, 64..128 in steps of
 //    16, chosen per launch so that the grid fills the SMs), so tensor-memory
