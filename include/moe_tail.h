@@ -81,6 +81,14 @@ const char* moe_status_string(int status);
  *
  * Products are exact; partial sums are FP32 (tensor-core accumulate), so
  * |logits - exact| is a small multiple of 2^-24 * sum_h |x * w|.
+ *
+ * Batches of more than 64 tokens (H >= 64) run a pipelined tensor-memory
+ * kernel whose waits are bounded (about two seconds each); if one runs out,
+ * the logits of that launch's affected 128-expert x token tiles are written
+ * as NaN (a quiet NaN in every element of the tile) and the call still
+ * returns MOE_OK, as the launch was made.  NaN logits then give unspecified
+ * ids downstream; a caller that must tell them from bad inputs checks the
+ * logits for NaN.
  */
 int moe_router_logits_fp32(const void* x_bf16, const void* w_gate_bf16, float* logits_out,
                            int64_t T, int64_t H, int64_t E, cudaStream_t stream);
@@ -169,6 +177,17 @@ int moe_tail_fused(const float* logits, int64_t E, int32_t k, float routed_scale
  * MOE_OK, or MOE_ERR_INVALID_ARG for stage < -1.  Not for production use.
  */
 int moe_debug_withhold_stream_stage(int32_t stage);
+
+/*
+ * Test hook of the launch-error path; no counterpart on the pages.  With
+ * on = 1 the next kernel launch made by any entry point asks the CUDA
+ * runtime for more dynamic shared memory than a thread block may have; the
+ * runtime refuses it before anything runs (a launch-configuration error, not
+ * a sticky one), the entry point returns MOE_ERR_CUDA, and later calls run
+ * normally.  on = 0 cancels a pending request.  Returns MOE_OK, or
+ * MOE_ERR_INVALID_ARG for any other value.  Not for production use.
+ */
+int moe_debug_fail_next_launch(int32_t on);
 
 /*
  * Test hook of the launch-shape choice of the tensor-memory router (batches

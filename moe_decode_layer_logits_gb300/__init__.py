@@ -23,6 +23,7 @@ from ._lib import MoeTailError, check, lib
 
 __all__ = [
     "moe_debug_withhold_stream_stage",
+    "moe_debug_fail_next_launch",
     "moe_debug_router_tc_shape",
     "moe_router_logits_fp32",
     "moe_topk_route",
@@ -140,6 +141,13 @@ def moe_debug_withhold_stream_stage(stage):
     leaves stage `stage` of its first CTA uncopied, so that CTA's wait runs
     out and MOE_FLAG_TIMEOUT is set; -1 cancels the request."""
     check(lib().moe_debug_withhold_stream_stage(int(stage)), "moe_debug_withhold_stream_stage")
+
+
+def moe_debug_fail_next_launch(on=True):
+    """Test hook of the launch-error path: the next kernel launch of any entry
+    point is refused by the CUDA runtime (oversized shared-memory request),
+    so that call raises MoeTailError with MOE_ERR_CUDA; on=False cancels."""
+    check(lib().moe_debug_fail_next_launch(1 if on else 0), "moe_debug_fail_next_launch")
 
 
 def moe_debug_router_tc_shape(T, H, E, nsm, mc2, mc4, mc8):

@@ -37,6 +37,7 @@ SIGNATURES = {
     "moe_tail_fused": (ctypes.c_int, [_vp, _i64, _i32, _f32, _vp, _i64, _vp, _vp, _vp, _vp, _f32, _vp, _vp,
                                       _vp, _vp, _i64, _i64, _vp, _vp]),
     "moe_debug_withhold_stream_stage": (ctypes.c_int, [_i32]),
+    "moe_debug_fail_next_launch": (ctypes.c_int, [_i32]),
     "moe_debug_router_tc_shape": (ctypes.c_int, [_i64, _i64, _i64, _i32, _i32, _i32, _i32, _vp, _vp]),
 }
 

@@ -1,4 +1,7 @@
-// Status strings and the per-device attribute cache of the C ABI.
+// Status strings, the per-device attribute cache and the launch-error test
+// hook of the C ABI.
+#include <atomic>
+
 #include "host_util.h"
 
 namespace moe {
@@ -6,7 +9,12 @@ namespace moe {
 namespace {
 constexpr int kMaxDevices = 64;
 int g_sm_count[kMaxDevices] = {0};  // 0 = not queried yet (a benign race: every writer stores the same value)
+std::atomic<int> g_fail_next_launch{0};
 }  // namespace
+
+bool take_injected_launch_failure() {
+  return g_fail_next_launch.load(std::memory_order_relaxed) != 0 && g_fail_next_launch.exchange(0) != 0;
+}
 
 int sm_count() {
   int dev = 0;
@@ -31,4 +39,10 @@ extern "C" const char* moe_status_string(int status) {
     case MOE_ERR_BAD_INDEX: return "MOE_ERR_BAD_INDEX: an expanded-index map entry was out of range";
     default: return "unknown moe status";
   }
+}
+
+extern "C" int moe_debug_fail_next_launch(int32_t on) {
+  if (on != 0 && on != 1) return MOE_ERR_INVALID_ARG;
+  moe::g_fail_next_launch.store(on);
+  return MOE_OK;
 }

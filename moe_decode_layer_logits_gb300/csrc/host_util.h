@@ -21,6 +21,17 @@ inline int launch_status() {
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Test hook of the launch-error path (moe_debug_fail_next_launch): true once
+// after a request, taken by the next launch of any entry point.
+bool take_injected_launch_failure();
+
+// Dynamic shared memory of a launch: `bytes`, or, when a launch failure was
+// requested, more than any block may have, so that the runtime refuses the
+// launch before anything runs and the entry point returns MOE_ERR_CUDA.
+inline size_t launch_smem(size_t bytes) {
+  return take_injected_launch_failure() ? (static_cast<size_t>(1) << 22) : bytes;
+}
+
 // Launch attribute that lets a kernel start while the previous kernel on the
 // stream finishes (the kernels wait on the dependency before touching memory).
 inline cudaLaunchAttribute pdl_attribute() {

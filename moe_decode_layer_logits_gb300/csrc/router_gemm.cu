@@ -176,7 +176,7 @@ static cudaError_t launch_router(const uint16_t* x, const uint16_t* W, float* lo
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(e_tiles, t_tiles, S);
   cfg.blockDim = dim3(WARPS * 32, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = launch_smem(0);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0] = pdl_attribute();

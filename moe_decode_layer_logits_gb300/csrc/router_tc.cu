@@ -438,7 +438,7 @@ static cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw, float
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((T + BNT - 1) / BNT, (E + kTcBM - 1) / kTcBM, S);
   cfg.blockDim = dim3(kTcThreads, 1, 1);
-  cfg.dynamicSmemBytes = tc_smem_bytes<BNT>();
+  cfg.dynamicSmemBytes = launch_smem(tc_smem_bytes<BNT>());
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0] = pdl_attribute();

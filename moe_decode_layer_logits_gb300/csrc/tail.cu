@@ -139,10 +139,10 @@ tail_kernel(const TailParams p) {
     int m = map_raw;
     if (m < 0 || static_cast<int64_t>(m) >= p.n_rows) {
       if (p.err_flag) atomicOr(p.err_flag, MOE_FLAG_BAD_INDEX);
-      m = -1;  // never dereferenced; the row counts as zero
+      m = -1;  // never dereferenced: the row reads as zeros and its weight is 0
     }
     map_s[tid] = m;
-    if (!ROUTE) w_s[tid] = __uint_as_float(w_raw);
+    if (!ROUTE) w_s[tid] = m < 0 ? 0.f : __uint_as_float(w_raw);
   }
   __syncthreads();
 
@@ -173,7 +173,7 @@ tail_kernel(const TailParams p) {
         float w;
         route_select<KEYS>(keys, k, p.scale, id, w);
         if (tid < k) {
-          w_s[tid] = w;
+          w_s[tid] = map_s[tid] < 0 ? 0.f : w;  // an unusable slot adds exactly nothing
           if (rank == 0) {
             const int64_t o = static_cast<int64_t>(t) * k + tid;
             if (p.ids_out) p.ids_out[o] = id;
@@ -363,12 +363,20 @@ __device__ __forceinline__ int checked_entry(const TailParams& p, int m) {
   return m;
 }
 
+// Longest row the stream kernel takes (four 16-byte vectors per consumer thread).
+constexpr int kStreamMaxH = 4 * kStreamConsumers * 8;
+
+// Source of the expert-row piece of a slot whose map entry names no row: a
+// row of zeros (never written), so with its weight set to 0 the slot adds
+// exactly nothing, as in tail_kernel, whatever the other inputs hold.
+__device__ __align__(128) uint16_t g_zero_row[kStreamMaxH];
+
 // Source row of piece l of token t's stage: slots 0..k-1 (expert rows through
-// the map; an unusable slot reads the residual row instead and has weight 0),
-// then shared, the R partials and the residual.
+// the map; an unusable slot reads the zero row and has weight 0), then shared,
+// the R partials and the residual.
 __device__ __forceinline__ const uint16_t* stream_piece(const TailParams& p, int64_t t, int l, int rows, int slot_row) {
   const int64_t roff = t * p.H;
-  if (l < p.k) return slot_row >= 0 ? p.rows + static_cast<int64_t>(slot_row) * p.H : p.residual + roff;
+  if (l < p.k) return slot_row >= 0 ? p.rows + static_cast<int64_t>(slot_row) * p.H : g_zero_row;
   if (p.shared && l == p.k) return p.shared + roff;
   if (l < rows - 1) {
     const int r = l - p.k - (p.shared ? 1 : 0);
@@ -382,7 +390,7 @@ __device__ __forceinline__ const uint16_t* stream_piece(const TailParams& p, int
 __device__ __forceinline__ void stream_prefetch_token(const TailParams& p, int64_t t, int rows, int slot_row) {
   const int lane = threadIdx.x & 31;
   for (int l = lane; l < rows; l += 32)
-    prefetch_l2(stream_piece(p, t, l, rows, slot_row), static_cast<uint32_t>(p.H) * 2u);
+    if (l >= p.k || slot_row >= 0) prefetch_l2(stream_piece(p, t, l, rows, slot_row), static_cast<uint32_t>(p.H) * 2u);
 }
 
 template <int VPT, int EPL>
@@ -702,7 +710,7 @@ static cudaError_t launch_tail_v(const TailParams& p, int T, const TailLaunch& L
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.cs, T, 1);
   cfg.blockDim = dim3(L.threads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = launch_smem(0);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0] = pdl_attribute();
@@ -765,7 +773,7 @@ static cudaError_t launch_stream_v(const TailParams& p, int T, const StreamShape
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kStreamThreads, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(sh.nstages) * sh.stage_bytes;
+  cfg.dynamicSmemBytes = launch_smem(static_cast<size_t>(sh.nstages) * sh.stage_bytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
   cfg.attrs = attr;
@@ -787,7 +795,7 @@ static cudaError_t launch_stream_e(const TailParams& p, int T, const StreamShape
 // The stream kernel takes batches of at least two tokens per SM whose rows fit
 // four vectors per consumer thread.
 static bool use_stream(int64_t T, int H, int rows, int nsm, StreamShape& sh) {
-  return T >= 2 * static_cast<int64_t>(nsm) && H / 8 <= 4 * kStreamConsumers && stream_shape(H, rows, sh);
+  return T >= 2 * static_cast<int64_t>(nsm) && H <= kStreamMaxH && stream_shape(H, rows, sh);
 }
 
 // Test hook of the bounded waits (moe_debug_withhold_stream_stage): a stage

@@ -31,6 +31,7 @@ static cudaError_t launch_route(const float* logits, int32_t* ids, float* w, int
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((T + kRouteWarps - 1) / kRouteWarps), 1, 1);
   cfg.blockDim = dim3(kRouteWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = launch_smem(0);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
   cfg.attrs = attr;

@@ -52,15 +52,35 @@ def tail_deltas(ref, n_ops, gamma, eps, extra_abs_r=None):
     return dr * 1.01, dn * 1.01
 
 
+# Per-case statistics of every BF16 comparison, printed at the end of the run
+# (tests/conftest.py, terminal summary): how close each output came and how
+# many elements needed the FP32 widening at all.
+STATS = []
+EXTRA = []  # free-form lines (e.g. rows a chain test could not compare one to one)
+
+
 def check_bf16(name, gpu_bits, ref_bits, ref_val, delta, max_widened_frac=0.01):
-    """Assert |bf16(gpu) - bf16(ref)| <= ulp + delta everywhere; returns stats."""
+    """Assert |bf16(gpu) - bf16(ref)| <= ulp + delta everywhere; returns stats.
+
+    The stats (also appended to STATS): the largest difference in BF16 ulps,
+    the number and fraction of elements more than one ulp away (they passed
+    only through delta), the fraction bit-identical to the oracle and the
+    fraction of elements whose tolerance was widened at all (delta > ulp/2).
+    """
     g = O.bf16_bits_to_f64(gpu_bits)
     o = O.bf16_bits_to_f64(ref_bits)
     ulp = np.maximum(O.bf16_ulp(o), O.bf16_ulp(ref_val))
     diff = np.abs(g - o)
     tol = ulp + delta
     bad = ~(diff <= tol)
-    widened = np.mean(delta > 0.5 * ulp)
+    widened = float(np.mean(delta > 0.5 * ulp)) if delta.size else 0.0
+    above = int(np.sum(diff > ulp))
+    st = {"case": name, "n": int(diff.size),
+          "max_ulps": float(np.max(diff / ulp)) if diff.size else 0.0,
+          "above_1ulp": above, "above_1ulp_frac": above / max(1, diff.size),
+          "exact_frac": float(np.mean(diff == 0)) if diff.size else 1.0,
+          "widened_frac": widened, "widened_cap": float(max_widened_frac)}
+    STATS.append(st)
     if bad.any():
         idx = np.argwhere(bad)[:5]
         raise AssertionError(
@@ -68,6 +88,4 @@ def check_bf16(name, gpu_bits, ref_bits, ref_val, delta, max_widened_frac=0.01):
             f"gpu {g[tuple(idx[0])]!r} oracle {o[tuple(idx[0])]!r} exact {ref_val[tuple(idx[0])]!r} "
             f"tol {tol[tuple(idx[0])]!r}")
     assert widened <= max_widened_frac, f"{name}: tolerance widened on {widened:.4%} of elements"
-    return {"max_ulps": float(np.max(diff / ulp)) if diff.size else 0.0,
-            "exact_frac": float(np.mean(diff == 0)) if diff.size else 1.0,
-            "widened_frac": float(widened)}
+    return st

@@ -190,6 +190,14 @@ def test_withhold_hook_argument_check(lib):
     assert lib.moe_debug_withhold_stream_stage(-1) == L.MOE_OK
 
 
+def test_fail_next_launch_hook_argument_check(lib):
+    # host-only: a request is stored (and cancelled here) for the next launch
+    assert lib.moe_debug_fail_next_launch(2) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_debug_fail_next_launch(-1) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_debug_fail_next_launch(1) == L.MOE_OK
+    assert lib.moe_debug_fail_next_launch(0) == L.MOE_OK
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     import moe_decode_layer_logits_gb300 as M

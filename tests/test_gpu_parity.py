@@ -13,6 +13,8 @@ import pytest
 import torch
 
 import oracle as O
+import _tol
+from _guard import Guarded, check_all
 from _tol import check_bf16, route_weight_tol, tail_deltas
 from moe_decode_layer_logits_gb300.inputs import draw_bf16, tail_case
 
@@ -68,7 +70,10 @@ def test_router_logits(M, T, H, E):
     x = draw_bf16(rng, (T, H), 1.0)
     w = draw_bf16(rng, (E, H), 0.02)
     L, A = O.router_logits(x, w)
-    g = M.moe_router_logits_fp32(dev(x), dev(w)).cpu().numpy().astype(np.float64)
+    out = Guarded((T, E), torch.float32)
+    M.moe_router_logits_fp32(dev(x), dev(w), logits_out=out.t)
+    out.check("logits")
+    g = out.t.cpu().numpy().astype(np.float64)
     err = np.abs(g - L)
     assert np.all(err <= 1e-5 * A + 1e-30), float(np.max(err / np.maximum(A, 1e-30)))
 
@@ -79,9 +84,10 @@ def test_router_logits_misaligned_output(M):
     rng = np.random.default_rng(103)
     x = draw_bf16(rng, (T, H), 1.0)
     w = draw_bf16(rng, (E, H), 0.02)
-    buf = torch.empty(T * E + 1, dtype=torch.float32, device="cuda")
-    out = buf[1:].view(T, E)
+    g = Guarded((T * E + 1,), torch.float32)
+    out = g.t[1:].view(T, E)
     M.moe_router_logits_fp32(dev(x), dev(w), logits_out=out)
+    g.check("logits")
     L, A = O.router_logits(x, w)
     assert np.all(np.abs(out.cpu().numpy().astype(np.float64) - L) <= 1e-5 * A)
 
@@ -91,7 +97,10 @@ def test_router_prefill_size_sampled(M):
     rng = np.random.default_rng(101)
     x = draw_bf16(rng, (T, H), 4.0)
     w = draw_bf16(rng, (E, H), 0.02)
-    g = M.moe_router_logits_fp32(dev(x), dev(w)).cpu().numpy().astype(np.float64)
+    out = Guarded((T, E), torch.float32)
+    M.moe_router_logits_fp32(dev(x), dev(w), logits_out=out.t)
+    out.check("logits")
+    g = out.t.cpu().numpy().astype(np.float64)
     rows = np.sort(rng.choice(T, 256, replace=False))
     rows[-1] = T - 1
     L, A = O.router_logits(x[rows], w)
@@ -105,8 +114,10 @@ def test_router_small_integers_exact(M):
     for T, H, E in [(64, 2048, 256), (3, 2048, 64), (33, 1000, 40), (1024, 2048, 256), (1130, 1016, 136)]:
         xi = rng.integers(-16, 17, size=(T, H))
         wi = rng.integers(-16, 17, size=(E, H))
-        g = M.moe_router_logits_fp32(dev(to_bf16_bits(xi)), dev(to_bf16_bits(wi))).cpu().numpy()
-        assert np.array_equal(g.astype(np.int64), xi @ wi.T)
+        out = Guarded((T, E), torch.float32)
+        M.moe_router_logits_fp32(dev(to_bf16_bits(xi)), dev(to_bf16_bits(wi)), logits_out=out.t)
+        out.check("logits")
+        assert np.array_equal(out.t.cpu().numpy().astype(np.int64), xi @ wi.T)
 
 
 # ---------------------------------------------------------------------------
@@ -120,7 +131,10 @@ ROUTE = [  # (T, E, k, scale)
 
 
 def _check_route(M, lg, k, scale):
-    ids_g, w_g = M.moe_topk_route(devf(lg), k, scale)
+    T = lg.shape[0]
+    gi, gw = Guarded((T, k), torch.int32), Guarded((T, k), torch.float32)
+    ids_g, w_g = M.moe_topk_route(devf(lg), k, scale, topk_ids=gi.t, topk_w=gw.t)
+    check_all(topk_ids=gi, topk_w=gw)
     ids_g = ids_g.cpu().numpy()
     w_g = w_g.cpu().numpy().astype(np.float64)
     ids, w32, w64 = O.topk_route(lg, k, scale)
@@ -168,8 +182,13 @@ def _run_finalize(M, c, residual_out=None, err_flag=None):
     sh = dev(c["shared"]) if c["shared"] is not None else None
     pa = dev(c["partials"]) if c["partials"] is not None else None
     res = dev(c["residual"])
+    T, H = c["residual"].shape
+    g_ro = None if residual_out == "alias" else Guarded((T, H), torch.bfloat16)
+    g_no = Guarded((T, H), torch.bfloat16)
     ro, no = M.moe_finalize_add_rmsnorm(rows, mp, w, sh, res, devf(c["gamma"]), c["eps"], partials=pa,
-                                        residual_out=res if residual_out == "alias" else None, err_flag=err_flag)
+                                        residual_out=res if residual_out == "alias" else g_ro.t,
+                                        normed_out=g_no.t, err_flag=err_flag)
+    check_all(residual_out=g_ro, normed_out=g_no)
     return bits(ro), bits(no)
 
 
@@ -190,6 +209,8 @@ FIN = [  # name, T, H, E, k, extra kwargs
     ("verify-4", 4, 6144, 256, 8, dict(seed=2)),
     ("verify-12", 12, 6144, 256, 8, dict(seed=2, s=4.0)),
     ("verify-28", 28, 6144, 256, 8, dict(seed=2)),
+    ("verify-4-h2048", 4, 2048, 256, 8, dict(seed=2)),
+    ("verify-4-h2048-s4", 4, 2048, 256, 8, dict(seed=2, s=4.0)),
     ("verify-12-h2048", 12, 2048, 256, 8, dict(seed=2)),
     ("verify-28-h2048", 28, 2048, 256, 8, dict(seed=2, s=4.0)),
     ("prefill-512", 512, 6144, 256, 8, dict(seed=3)),
@@ -245,11 +266,11 @@ def test_finalize_full_size_sampled(M, T, kw):
     c = tail_case(T, 6144, 256, k, router=False, **kw)
     ro, no = _run_finalize(M, c)
     rng = np.random.default_rng(T)
-    tok = np.sort(rng.choice(T, 48, replace=False))
+    tok = np.sort(rng.choice(T, 512, replace=False))
     tok[0], tok[-1] = 0, T - 1
     ref = _oracle_tail(c, tok)
     _check_tail({**c, "shared": None if c["shared"] is None else c["shared"][tok]}, ref, ro[tok], no[tok],
-                tag=f"T={T}")
+                tag=f"finalize T={T} k={k} R={c['R']} (512 sampled rows)")
 
 
 def test_finalize_residual_out_may_alias_residual(M):
@@ -266,8 +287,10 @@ def test_finalize_bad_index_sets_flag_and_reads_zero(M, T):
     c["map"] = c["map"].copy()
     c["map"][1, 2] = n          # one past the end
     c["map"][4, 0] = -1         # negative
-    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gflag = Guarded((1,), torch.int32, fill=0)
+    flag = gflag.t
     ro, no = _run_finalize(M, c, err_flag=flag)
+    gflag.check("err_flag")
     assert int(flag.item()) & 1
     # the kernel never dereferences them: those rows count as zero
     w = c["topk_w"].copy()
@@ -283,6 +306,95 @@ def test_finalize_bad_index_sets_flag_and_reads_zero(M, T):
     c2 = tail_case(6, 1024, 16, 4, router=False, seed=22)
     _run_finalize(M, c2, err_flag=flag)
     assert int(flag.item()) == 0
+
+
+@pytest.mark.parametrize("T", [6, 400])
+def test_unusable_slot_adds_nothing_whatever_the_inputs(M, T):
+    """A slot whose map entry names no row adds exactly nothing on both tail
+    kernels (decode sizes and the persistent kernel): not 0 * inf, not
+    0 * NaN.  Token 1 has a bad slot whose weight is NaN and an infinite
+    residual element; token 2 a bad slot and a NaN residual element."""
+    c = tail_case(T, 1024, 16, 4, router=False, seed=41)
+    n = c["rows"].shape[0]
+    c["map"] = c["map"].copy()
+    c["topk_w"] = c["topk_w"].copy()
+    c["residual"] = c["residual"].copy()
+    c["map"][1, 2] = n + 5
+    c["topk_w"][1, 2] = np.nan
+    c["residual"][1, 100] = 0x7F80      # +inf
+    c["map"][2, 0] = -7
+    c["residual"][2, 300] = 0x7FC0      # NaN
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ro, no = _run_finalize(M, c, err_flag=flag)
+    assert int(flag.item()) & 1
+    # reference: the bad slots removed (weight 0 on row 0), on finite residuals
+    w = c["topk_w"].copy()
+    w[1, 2] = 0.0
+    w[2, 0] = 0.0
+    safe = c["map"].copy()
+    safe[1, 2] = 0
+    safe[2, 0] = 0
+    good = np.array([t for t in range(T) if t not in (1, 2)])
+    cc = {**c, "map": safe, "topk_w": w}
+    ref = _oracle_tail(cc, good)
+    _check_tail({**c, "shared": c["shared"][good]}, ref, ro[good], no[good], tag=f"unusable-slot T={T}")
+    # token 1: +inf where the residual is +inf, every other element as the oracle
+    fin = O.finalize_add_rmsnorm(c["rows"], safe[1:2], w[1:2], c["shared"][1:2], None,
+                                 np.where(np.arange(1024) == 100, 0, c["residual"][1]).astype(np.uint16)[None],
+                                 c["gamma"], c["eps"])
+    r1 = O.bf16_bits_to_f64(ro[1])
+    assert r1[100] == np.inf
+    other = np.arange(1024) != 100
+    assert np.all(np.abs(r1[other] - O.bf16_bits_to_f64(fin["residual_out"][0])[other]) <=
+                  O.bf16_ulp(O.bf16_bits_to_f64(fin["residual_out"][0])[other]) + 1e-30)
+    # the sum of squares is +inf: the normed row is 0 except NaN at the inf element
+    n1 = O.bf16_bits_to_f64(no[1])
+    assert np.isnan(n1[100]) and np.all(n1[other] == 0.0)
+    # token 2: NaN only where the residual is NaN in residual_out; normed all NaN
+    r2 = O.bf16_bits_to_f64(ro[2])
+    assert np.isnan(r2[300]) and np.all(np.isfinite(np.delete(r2, 300)))
+    assert np.all(np.isnan(O.bf16_bits_to_f64(no[2])))
+
+
+@pytest.mark.parametrize("what", ["router-decode", "router-tc", "route", "finalize-decode", "finalize-stream",
+                                  "fused-decode"])
+def test_refused_launch_returns_cuda_error_and_the_next_call_is_clean(M, what):
+    """A launch the CUDA runtime refuses (requested through the test hook:
+    an oversized shared-memory request, checked before anything runs) comes
+    back as MOE_ERR_CUDA; no error stays behind and the next call matches the
+    oracle."""
+    import moe_decode_layer_logits_gb300._lib as L
+    T = {"router-decode": 4, "router-tc": 256, "route": 9, "finalize-decode": 6, "finalize-stream": 400,
+         "fused-decode": 6}[what]
+    c = tail_case(T, 1024, 64, 4, seed=42, logits=True, router=what.startswith("router"))
+
+    def call():
+        if what.startswith("router"):
+            return M.moe_router_logits_fp32(dev(c["x"]), dev(c["w_gate"]))
+        if what == "route":
+            return M.moe_topk_route(devf(c["logits"]), 4, c["scale"])
+        if what.startswith("finalize"):
+            return _run_finalize(M, c)
+        return _run_fused(M, c)
+
+    M.moe_debug_fail_next_launch(True)
+    with pytest.raises(L.MoeTailError) as ei:
+        call()
+    assert ei.value.status == L.MOE_ERR_CUDA
+    torch.cuda.synchronize()  # nothing sticky: the context still works
+    out = call()
+    if what.startswith("router"):
+        L_, A = O.router_logits(c["x"], c["w_gate"])
+        assert np.all(np.abs(out.cpu().numpy().astype(np.float64) - L_) <= 1e-5 * A)
+    elif what == "route":
+        ids, _, _ = O.topk_route(c["logits"], 4, c["scale"])
+        assert np.array_equal(out[0].cpu().numpy(), ids)
+    elif what.startswith("finalize"):
+        _check_tail(c, _oracle_tail(c), out[0], out[1], tag=f"after refused launch ({what})")
+    else:
+        ro, no, ids, w = out
+        _check_fused_outputs(c, c["logits"], bits(ro), bits(no), ids.cpu().numpy(),
+                             w.cpu().numpy().astype(np.float64), tag=f"after refused launch ({what})")
 
 
 def test_stream_wait_runs_out_and_the_next_launch_is_clean(M):
@@ -326,21 +438,32 @@ def test_row_permutation_is_bitwise_invariant(M):
 # router-less fused tail
 # ---------------------------------------------------------------------------
 
-def _run_fused(M, c, want_route=True):
-    return M.moe_tail_fused(devf(c["logits"]), c["k"], c["scale"], dev(c["rows"]), torch.from_numpy(c["map"]).cuda(),
-                            dev(c["shared"]) if c["shared"] is not None else None, dev(c["residual"]),
-                            devf(c["gamma"]), c["eps"], want_route=want_route)
+def _run_fused(M, c, want_route=True, logits=None):
+    T, H = c["residual"].shape
+    k = c["k"]
+    g_ro, g_no = Guarded((T, H), torch.bfloat16), Guarded((T, H), torch.bfloat16)
+    g_id = Guarded((T, k), torch.int32) if want_route else None
+    g_w = Guarded((T, k), torch.float32) if want_route else None
+    out = M.moe_tail_fused(devf(c["logits"]) if logits is None else logits, k, c["scale"], dev(c["rows"]),
+                           torch.from_numpy(c["map"]).cuda(), dev(c["shared"]) if c["shared"] is not None else None,
+                           dev(c["residual"]), devf(c["gamma"]), c["eps"], residual_out=g_ro.t, normed_out=g_no.t,
+                           topk_ids=None if g_id is None else g_id.t, topk_w=None if g_w is None else g_w.t,
+                           want_route=want_route)
+    check_all(residual_out=g_ro, normed_out=g_no, topk_ids=g_id, topk_w=g_w)
+    return out
 
 
-def _check_fused(M, c, tok=None, tag=""):
-    ro, no, ids, w = _run_fused(M, c)
-    ro, no, ids, w = bits(ro), bits(no), ids.cpu().numpy(), w.cpu().numpy().astype(np.float64)
+def _check_fused_outputs(c, lg, ro, no, ids, w, tok=None, tag=""):
+    """Routing and tail of one fused launch against the oracle, both fed the
+    same FP32 logits `lg` [T, E]: ids bit-exact, weights within the FP32
+    bound of the GPU formula, outputs within one BF16 ulp (+ the FP32 bound,
+    including the weights' allowed error)."""
     sl = slice(None) if tok is None else tok
-    lg = c["logits"][sl]
+    lg = lg[sl]
     rids, rw32, rw64 = O.topk_route(lg, c["k"], c["scale"])
-    assert np.array_equal(ids[sl], rids)
+    assert np.array_equal(ids[sl], rids), f"{tag}: ids differ"
     wtol = route_weight_tol(lg, rids, rw64)
-    assert np.all(np.abs(w[sl] - rw64) <= wtol)
+    assert np.all(np.abs(w[sl] - rw64) <= wtol), f"{tag}: weights off"
     sh = None if c["shared"] is None else c["shared"][sl]
     ref = O.finalize_add_rmsnorm(c["rows"], c["map"][sl], rw32, sh, None, c["residual"][sl], c["gamma"], c["eps"])
     # the GPU weights may differ from the oracle's by wtol (+ half a binary32 ulp of rounding)
@@ -352,13 +475,25 @@ def _check_fused(M, c, tok=None, tag=""):
     return _check_tail({**c, "shared": sh}, ref, ro[sl], no[sl], extra_abs_r=extra, tag=tag)
 
 
+def _check_fused(M, c, tok=None, tag=""):
+    ro, no, ids, w = _run_fused(M, c)
+    return _check_fused_outputs(c, c["logits"], bits(ro), bits(no), ids.cpu().numpy(),
+                                w.cpu().numpy().astype(np.float64), tok=tok, tag=tag)
+
+
 FUSED = [  # name, T, H, E, k, kw
     ("tiny", 4, 2048, 64, 4, dict(scale=1.0, seed=0)),
+    ("tiny-s4", 4, 2048, 64, 4, dict(scale=1.0, seed=0, s=4.0)),
     ("decode-1", 1, 6144, 256, 8, dict(seed=1)),
     ("decode-4", 4, 6144, 256, 8, dict(seed=1, s=4.0)),
     ("decode-64", 64, 6144, 256, 8, dict(seed=1)),
+    ("verify-4", 4, 6144, 256, 8, dict(seed=2)),
+    ("verify-12", 12, 6144, 256, 8, dict(seed=2, s=4.0)),
     ("verify-28", 28, 6144, 256, 8, dict(seed=2)),
+    ("verify-4-h2048", 4, 2048, 256, 8, dict(seed=2)),
+    ("verify-4-h2048-s4", 4, 2048, 256, 8, dict(seed=2, s=4.0)),
     ("verify-12-h2048", 12, 2048, 256, 8, dict(seed=2)),
+    ("verify-28-h2048", 28, 2048, 256, 8, dict(seed=2, s=4.0)),
     ("prefill-512", 512, 6144, 256, 8, dict(seed=3)),
     ("ragged", 37, 2056, 72, 3, dict(seed=8)),
     ("no-shared", 5, 1024, 1024, 32, dict(seed=9, shared=False)),
@@ -381,9 +516,9 @@ def test_tail_fused(M, name, T, H, E, k, kw):
 def test_tail_fused_full_size_sampled(M, T):
     c = tail_case(T, 6144, 256, 8, router=False, logits=True, weights=False, seed=3)
     rng = np.random.default_rng(T + 1)
-    tok = np.sort(rng.choice(T, 48, replace=False))
+    tok = np.sort(rng.choice(T, 512, replace=False))
     tok[0], tok[-1] = 0, T - 1
-    _check_fused(M, c, tok=tok, tag=f"T={T}")
+    _check_fused(M, c, tok=tok, tag=f"fused T={T} (512 sampled rows)")
 
 
 def test_tail_fused_without_route_outputs(M):
@@ -409,51 +544,108 @@ def test_tail_fused_matches_route_then_finalize_bitwise(M):
 # the whole decode step: router -> route -> tail, and CUDA-graph replay
 # ---------------------------------------------------------------------------
 
-def _decode_step(M, g, c, fused):
-    logits = M.moe_router_logits_fp32(g["x"], g["w_gate"])
+def _decode_step(M, g, c, fused, out=None):
+    """One decode layer through the C ABI; `out` (optional) holds Guarded
+    output buffers keyed logits / ids / w / ro / no."""
+    o = out or {}
+    t = lambda n: o[n].t if n in o else None
+    logits = M.moe_router_logits_fp32(g["x"], g["w_gate"], logits_out=t("logits"))
     if fused:
         ro, no, ids, w = M.moe_tail_fused(logits, c["k"], c["scale"], g["rows"], g["map"], g["shared"],
-                                          g["residual"], g["gamma"], c["eps"])
+                                          g["residual"], g["gamma"], c["eps"], residual_out=t("ro"),
+                                          normed_out=t("no"), topk_ids=t("ids"), topk_w=t("w"))
     else:
-        ids, w = M.moe_topk_route(logits, c["k"], c["scale"])
-        ro, no = M.moe_finalize_add_rmsnorm(g["rows"], g["map"], w, g["shared"], g["residual"], g["gamma"], c["eps"])
+        ids, w = M.moe_topk_route(logits, c["k"], c["scale"], topk_ids=t("ids"), topk_w=t("w"))
+        ro, no = M.moe_finalize_add_rmsnorm(g["rows"], g["map"], w, g["shared"], g["residual"], g["gamma"], c["eps"],
+                                            residual_out=t("ro"), normed_out=t("no"))
     return logits, ids, w, ro, no
 
 
-@pytest.mark.parametrize("T,fused", [(1, True), (4, False), (64, True), (64, False), (28, True)])
-def test_decode_chain(M, T, fused):
-    c = tail_case(T, 6144, 256, 8, seed=1, weights=False)
+# The pages' unit-test matrix crosses 1 / 4 / 64 tokens with hidden sizes 2048
+# and 6144; the MTP verify batches are 4 / 12 / 28 tokens at both sizes.
+CHAIN = [  # T, H, fused, seed
+    (1, 6144, True, 1), (4, 6144, False, 1), (64, 6144, True, 1), (64, 6144, False, 1),
+    (12, 6144, False, 2), (28, 6144, True, 2),
+    (1, 2048, True, 1), (4, 2048, True, 2), (4, 2048, False, 2), (12, 2048, True, 2), (28, 2048, False, 2),
+    (64, 2048, True, 1),
+]
+# Rows whose top-(k+1) order the logits' measured error could flip: none in an
+# FP32-accumulation emulation of these cases on the CPU; a few percent allowed.
+CHAIN_MAX_UNCLEAR = 0.05
+# With the weight tolerance taken from the logits' measured error (not from the
+# 1e-5 * sum|x w| bound), the FP32 widening reaches about 0.1% of elements in
+# the same emulation: the usual 1% cap holds end to end too.
+CHAIN_E2E_WIDENED_CAP = 0.01
+
+
+@pytest.mark.parametrize("T,H,fused,seed", CHAIN, ids=[f"T{t}-H{h}-{'fused' if f else 'three-launch'}"
+                                                       for t, h, f, _ in CHAIN])
+def test_decode_chain(M, T, H, fused, seed):
+    """Router -> top-k -> tail on the GPU, checked step by step and end to end.
+
+    Step by step: the logits against the exact products (1e-5 * sum|x w|);
+    the routing and the tail against the oracle fed the GPU's own FP32
+    logits (ids bit-exact, outputs within one BF16 ulp + the FP32 bound).
+    End to end: against the oracle chain on the exact logits; rows whose
+    top-(k+1) order is decided by less than the logits' measured error may
+    pick another valid expert set, so those rows are checked for validity
+    only and counted."""
+    c = tail_case(T, H, 256, 8, seed=seed, weights=False)
+    k = c["k"]
     g = {"x": dev(c["x"]), "w_gate": dev(c["w_gate"]), "rows": dev(c["rows"]), "map": torch.from_numpy(c["map"]).cuda(),
          "shared": dev(c["shared"]), "residual": dev(c["residual"]), "gamma": devf(c["gamma"])}
-    logits, ids, w, ro, no = _decode_step(M, g, c, fused)
+    out = {"logits": Guarded((T, 256), torch.float32), "ids": Guarded((T, k), torch.int32),
+           "w": Guarded((T, k), torch.float32), "ro": Guarded((T, H), torch.bfloat16),
+           "no": Guarded((T, H), torch.bfloat16)}
+    logits, ids, w, ro, no = _decode_step(M, g, c, fused, out)
+    check_all(**out)
+    tag = f"chain T={T} H={H} {'fused' if fused else '3-launch'}"
+    # (1) logits
     L, A = O.router_logits(c["x"], c["w_gate"])
-    lg = logits.cpu().numpy().astype(np.float64)
-    ltol = 1e-5 * A
-    assert np.all(np.abs(lg - L) <= ltol)
-    # oracle route on its own logits; rows whose top-(k+1) order is decided by
-    # less than twice the logit tolerance may legitimately differ
-    rids, rw32, rw64 = O.topk_route(L.astype(np.float32), c["k"], c["scale"])
-    srt = -np.sort(-L, axis=1)[:, : c["k"] + 1]
+    lg32 = logits.cpu().numpy()
+    lg = lg32.astype(np.float64)
+    assert np.all(np.abs(lg - L) <= 1e-5 * A), f"{tag}: logits off"
+    ids, w = ids.cpu().numpy(), w.cpu().numpy().astype(np.float64)
+    ro, no = bits(ro), bits(no)
+    # (2)+(3) step by step: the oracle routes the GPU's logits
+    if fused:
+        _check_fused_outputs(c, lg32, ro, no, ids, w, tag=tag + " (oracle on GPU logits)")
+    else:
+        rids, _, rw64 = O.topk_route(lg32, k, c["scale"])
+        assert np.array_equal(ids, rids), f"{tag}: ids differ"
+        assert np.all(np.abs(w - rw64) <= route_weight_tol(lg32, rids, rw64)), f"{tag}: weights off"
+        ref = O.finalize_add_rmsnorm(c["rows"], c["map"], w.astype(np.float32), c["shared"], None, c["residual"],
+                                     c["gamma"], c["eps"])
+        _check_tail(c, ref, ro, no, tag=tag + " (oracle on GPU weights)")
+    # (4) end to end against the exact logits
+    d = np.abs(lg - L).max(axis=1) + 2.0 ** -24 * np.abs(L).max(axis=1)  # logit error incl. the FP32 cast
+    eids, ew32, ew64 = O.topk_route(L.astype(np.float32), k, c["scale"])
+    srt = -np.sort(-L, axis=1)[:, : k + 1]
     gaps = np.abs(np.diff(srt, axis=1)).min(axis=1)
-    clear = gaps > 2 * ltol.max(axis=1) + 1e-6
-    ids = ids.cpu().numpy()
-    assert np.array_equal(ids[clear], rids[clear])
-    assert clear.mean() > 0.5
-    # weights: exp of logits that differ by <= ltol, plus the route tolerance
-    w = w.cpu().numpy().astype(np.float64)
-    wtol = route_weight_tol(L.astype(np.float32), rids, rw64) + rw64 * (np.exp(4 * ltol.max(axis=1, keepdims=True)) - 1)
-    assert np.all(np.abs(w[clear] - rw64[clear]) <= wtol[clear])
-    ref = O.finalize_add_rmsnorm(c["rows"], c["map"], rw32, c["shared"], None, c["residual"], c["gamma"], c["eps"])
-    rows = O.bf16_bits_to_f64(c["rows"])
-    extra = np.zeros_like(ref["r"])
-    for j in range(c["k"]):
-        extra += (wtol[:, j:j + 1] + rw64[:, j:j + 1] * 2.0 ** -24) * np.abs(rows[c["map"][:, j]])
-    cc = {**c, "shared": c["shared"][clear], "R": 0}
-    sub = {kk: (v[clear] if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] == T else v) for kk, v in ref.items()}
-    # the weight tolerance inherits the logit bound 1e-5 * sum|x w|, so this
-    # end-to-end check is wider than the per-step checks above
-    _check_tail(cc, sub, bits(ro)[clear], bits(no)[clear], extra_abs_r=extra[clear], tag=f"chain T={T}",
-                max_widened_frac=1.0)
+    clear = gaps > 2 * d + 1e-6 * np.abs(srt[:, :1]).ravel()
+    assert np.array_equal(ids[clear], eids[clear]), f"{tag}: ids differ from the exact-logit route"
+    for t in np.nonzero(~clear)[0]:  # another valid top-k within the logit error
+        chosen = L[t, ids[t]]
+        rest = np.delete(L[t], ids[t])
+        assert len(set(ids[t].tolist())) == k and chosen.min() >= rest.max() - 2 * d[t], f"{tag}: row {t} invalid"
+    unclear = float(np.mean(~clear))
+    _tol.EXTRA.append(f"{tag}: {int((~clear).sum())} of {T} rows ({unclear:.1%}) have a top-(k+1) gap below the "
+                      f"measured logit error; checked for validity only")
+    assert unclear <= CHAIN_MAX_UNCLEAR, f"{tag}: {unclear:.1%} rows unclear"
+    if clear.any():
+        # weights: a logit error d moves w_j by at most a factor exp(+-2d)
+        wtol = route_weight_tol(lg32, ids, ew64) + ew64 * (np.exp(2 * d[:, None]) - 1.0)
+        assert np.all(np.abs(w[clear] - ew64[clear]) <= wtol[clear]), f"{tag}: weights off (exact logits)"
+        ref = O.finalize_add_rmsnorm(c["rows"], c["map"], ew32, c["shared"], None, c["residual"], c["gamma"], c["eps"])
+        rows = O.bf16_bits_to_f64(c["rows"])
+        extra = np.zeros_like(ref["r"])
+        for j in range(k):
+            extra += (wtol[:, j:j + 1] + ew64[:, j:j + 1] * 2.0 ** -24) * np.abs(rows[c["map"][:, j]])
+        cc = {**c, "shared": c["shared"][clear], "R": 0}
+        sub = {kk: (v[clear] if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] == T else v)
+               for kk, v in ref.items()}
+        _check_tail(cc, sub, ro[clear], no[clear], extra_abs_r=extra[clear], tag=tag + " (exact logits)",
+                    max_widened_frac=CHAIN_E2E_WIDENED_CAP)
 
 
 def test_cuda_graph_replay_matches_eager(M):
