@@ -82,6 +82,11 @@ const char* moe_status_string(int status);
  * Products are exact; partial sums are FP32 (tensor-core accumulate), so
  * |logits - exact| is a small multiple of 2^-24 * sum_h |x * w|.
  *
+ * w_gate is a model parameter: the kernel starts copying it into shared
+ * memory before it waits for the previous kernel on the stream, so it must
+ * not be written by a kernel that may still be running on `stream` when this
+ * call is made (x may be: it is read only after that wait).
+ *
  * Batches of more than 64 tokens (H >= 64) run a pipelined tensor-memory
  * kernel whose waits are bounded (about two seconds each); if one runs out,
  * the logits of that launch's affected 128-expert x token tiles are written

@@ -108,31 +108,6 @@ __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Sum of one float per thread over the whole thread-block cluster, in one
-// exchange: every warp pushes its sum into slot [rank * nwarps + warp] of
-// every CTA (distributed shared memory), one barrier publishes the stores,
-// and each thread adds the cluster size x nwarps slots in that fixed order,
-// so all CTAs get the same total, bit for bit.  The caller has arrived on the
-// cluster barrier once (cluster_arrive_relaxed) since the kernel started;
-// every thread of every CTA in the cluster must call this.  `slots` holds at
-// least cluster size x nwarps floats.
-__device__ __forceinline__ float cluster_block_sum(float v, float* slots) {
-  cg::cluster_group cluster = cg::this_cluster();
-  const unsigned n = cluster.num_blocks();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwarps = (blockDim.x + 31) >> 5;
-  v = warp_sum(v);
-  cluster_wait_acquire();  // every peer has started: its shared memory is live
-  if (static_cast<unsigned>(lane) < n)
-    *cluster.map_shared_rank(slots + cluster.block_rank() * nwarps + warp, lane) = v;
-  cluster_arrive_release();
-  cluster_wait_acquire();
-  float s = 0.f;
-  for (int i = 0; i < static_cast<int>(n) * nwarps; ++i) s += slots[i];
-  return s;
-}
-
-
 }  // namespace moe
 
 namespace moe {
@@ -175,6 +150,58 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, ui
       : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
+}
+
+// Shared::cluster address of `p` (this CTA's shared memory) in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+
+// Store one float into a cluster peer's shared memory; the store counts 4
+// bytes on that peer's mbarrier (both given as shared::cluster addresses), so
+// the peer learns of it by waiting on its own barrier -- no cluster barrier.
+__device__ __forceinline__ void st_async_f32(uint32_t remote, float v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(remote), "f"(v),
+               "r"(remote_bar)
+               : "memory");
+}
+
+// Probes of phase `parity` of `bar` until it completes; false after about
+// `max_probes` probes of up to 1 us each.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int max_probes) {
+  for (int it = 0; it < max_probes; ++it)
+    if (mbar_try_wait(bar, parity, 1000)) return true;
+  return false;
+}
+
+// Sum of one float per thread over the whole thread-block cluster, delivered
+// by asynchronous remote stores: every warp sends its sum to slot
+// [rank * nwarps + warp] of every CTA of the cluster, each store counted on
+// the receiving CTA's barrier `bar` (initialised with count 1 and made
+// visible to the cluster before the caller's first cluster_arrive_relaxed),
+// and each thread adds the cluster size x nwarps slots in that fixed order
+// once its own barrier has seen them all, so all CTAs get the same total, bit
+// for bit.  A CTA leaves only after every store into its shared memory has
+// landed.  Every thread of every CTA calls this once per launch; false (and
+// an unspecified total) if the wait ran out.
+__device__ __forceinline__ bool cluster_block_sum_async(float& v, float* slots, uint64_t* bar) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const unsigned n = cluster.num_blocks();
+  const unsigned rank = cluster.block_rank();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  v = warp_sum(v);
+  if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * nwarps * 4));
+  cluster_wait_acquire();  // every peer has started: its shared memory and barrier are live
+  if (static_cast<unsigned>(lane) < n)
+    st_async_f32(cluster_addr(slots + rank * nwarps + warp, lane), v, cluster_addr(bar, lane));
+  const bool ok = mbar_wait_bounded(bar, 0, 1 << 21);
+  float s = 0.f;
+  for (int i = 0; i < static_cast<int>(n) * nwarps; ++i) s += slots[i];
+  v = s;
+  return ok;
 }
 
 // L2 policy for data read exactly once (expert rows, activations).

@@ -8,8 +8,8 @@
 //    its warps split that slice again;
 //  - the CTAs that share an (expert, token) tile form a thread-block cluster
 //    (split-K over H) and add their partial tiles through distributed shared
-//    memory in ascending rank order -- deterministic, no atomics, no global
-//    scratch;
+//    memory (remote stores counted on the owner's mbarrier) in ascending rank
+//    order -- deterministic, no atomics, no global scratch;
 //  - each lane loads 16 contiguous bytes of a W row and of an x row per
 //    32-wide chunk of H and feeds them straight from registers into
 //    mma.m16n8k16 (W rows as the M side, tokens as the N side).  Within a
@@ -45,6 +45,16 @@ __device__ __forceinline__ void frag_to_tile(int i, int& e, int& t) {
   t = 8 * nt + 2 * (lane & 3) + (reg & 1);
 }
 
+// 16-byte asynchronous copy global -> shared (cp.async, L2 only); `full`
+// false copies nothing and zero-fills the 16 bytes.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool full) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(full ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 template <int NT, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32)
 router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, float* __restrict__ logits,
@@ -52,6 +62,10 @@ router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, fl
   constexpr int TILE = 16 * 8 * NT;  // outputs per tile
   __shared__ float red[WARPS][TILE];
   __shared__ float part[TILE];  // S > 1: part[src * per + i] = rank src's partial of output ib + i
+  // each lane's gate-weight fragments of its warp's first round, staged before
+  // the dependency wait (every thread reads back only its own slots)
+  __shared__ uint4 w_stage[WARPS][kRouterUnroll][2][32];
+  __shared__ uint64_t xbar;  // S > 1: completes when every CTA's partials of this CTA's outputs have landed
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
@@ -63,7 +77,13 @@ router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, fl
   const int wb = cb + (ce - cb) * warp / WARPS;
   const int we = cb + (ce - cb) * (warp + 1) / WARPS;
 
-  if (S > 1) cluster_arrive_relaxed();
+  if (S > 1) {
+    if (tid == 0) {
+      mbar_init(&xbar, 1);
+      mbar_init_fence();  // visible to the cluster's remote stores after the cluster barrier
+    }
+    cluster_arrive_relaxed();
+  }
   allow_dependent_launch();
   // While the previous kernel finishes: L2 prefetch of this CTA's slice of
   // the gate weight and, from the first expert tile, of the token rows of x
@@ -76,12 +96,24 @@ router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, fl
     else if (blockIdx.x == 0 && tid >= 32 && tid < 32 + 8 * NT && t0 + tid - 32 < T)  // once per slice of x
       prefetch_l2(x + static_cast<int64_t>(t0 + tid - 32) * H + h0, static_cast<uint32_t>((h1 - h0) * 2));
   }
-  grid_dependency_wait();
-
   const int eA = e0 + g, eB = e0 + g + 8;
   const bool okA = eA < E, okB = eB < E;
   const uint16_t* pA = W + static_cast<int64_t>(okA ? eA : 0) * H + 8 * q;
   const uint16_t* pB = W + static_cast<int64_t>(okB ? eB : 0) * H + 8 * q;
+  // The gate weight is a model parameter that no kernel still running on the
+  // stream writes, so its first round is copied into shared memory while the
+  // previous kernel finishes; only x is read after the dependency wait.
+  // Fragments outside W are zero-filled (the dummy source W is never read).
+#pragma unroll
+  for (int u = 0; u < kRouterUnroll; ++u) {
+    const int cc = wb + u;
+    const bool ok = cc < we && (cc * 32 + 8 * q) < H;
+    const int64_t off = static_cast<int64_t>(cc) * 32;
+    cp_async16(&w_stage[warp][u][0][lane], (ok && okA) ? static_cast<const void*>(pA + off) : W, ok && okA);
+    cp_async16(&w_stage[warp][u][1][lane], (ok && okB) ? static_cast<const void*>(pB + off) : W, ok && okB);
+  }
+  cp_async_commit();
+  grid_dependency_wait();
   const uint16_t* px[NT];
   bool okx[NT];
 #pragma unroll
@@ -96,18 +128,18 @@ router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, fl
   for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 
   const uint4 zero = make_uint4(0, 0, 0, 0);
-  for (int c = wb; c < we; c += kRouterUnroll) {
-    uint4 a[kRouterUnroll][2], b[kRouterUnroll][NT];
+  // one round: kRouterUnroll 32-wide chunks of H starting at chunk c
+  auto load_x = [&](int c, uint4 (&b)[kRouterUnroll][NT]) {
 #pragma unroll
     for (int u = 0; u < kRouterUnroll; ++u) {
       const int cc = c + u;
       const bool ok = cc < we && (cc * 32 + 8 * q) < H;
       const int64_t off = static_cast<int64_t>(cc) * 32;
-      a[u][0] = (ok && okA) ? ld_stream16(pA + off) : zero;
-      a[u][1] = (ok && okB) ? ld_stream16(pB + off) : zero;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) b[u][nt] = (ok && okx[nt]) ? ld_keep16(px[nt] + off) : zero;
     }
+  };
+  auto mma_round = [&](const uint4 (&a)[kRouterUnroll][2], const uint4 (&b)[kRouterUnroll][NT]) {
 #pragma unroll
     for (int u = 0; u < kRouterUnroll; ++u) {
 #pragma unroll
@@ -116,6 +148,30 @@ router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, fl
         mma_bf16_16816(acc[nt], a[u][0].z, a[u][1].z, a[u][0].w, a[u][1].w, b[u][nt].z, b[u][nt].w);
       }
     }
+  };
+  {  // first round: the gate weight from the fragments staged before the wait
+    uint4 a[kRouterUnroll][2], b[kRouterUnroll][NT];
+    load_x(wb, b);
+    cp_async_wait_all();  // this thread's own staged fragments
+#pragma unroll
+    for (int u = 0; u < kRouterUnroll; ++u) {
+      a[u][0] = w_stage[warp][u][0][lane];
+      a[u][1] = w_stage[warp][u][1][lane];
+    }
+    mma_round(a, b);
+  }
+  for (int c = wb + kRouterUnroll; c < we; c += kRouterUnroll) {
+    uint4 a[kRouterUnroll][2], b[kRouterUnroll][NT];
+#pragma unroll
+    for (int u = 0; u < kRouterUnroll; ++u) {
+      const int cc = c + u;
+      const bool ok = cc < we && (cc * 32 + 8 * q) < H;
+      const int64_t off = static_cast<int64_t>(cc) * 32;
+      a[u][0] = (ok && okA) ? ld_stream16(pA + off) : zero;
+      a[u][1] = (ok && okB) ? ld_stream16(pB + off) : zero;
+    }
+    load_x(c, b);
+    mma_round(a, b);
   }
 
 #pragma unroll
@@ -135,28 +191,31 @@ router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, fl
     return;
   }
   // split-K over the cluster: rank r owns outputs [r * per, (r + 1) * per); every
-  // CTA pushes its partial of those outputs into the owner's part[], then the
-  // owner adds the S partials in rank order
+  // CTA sends its partial of those outputs into the owner's part[] by remote
+  // stores counted on the owner's barrier, then the owner adds the S partials
+  // in rank order.  A CTA leaves only after every store into its shared
+  // memory has landed; if that wait ran out, its logits are written as NaN.
   cg::cluster_group cluster = cg::this_cluster();
   const int me = static_cast<int>(cluster.block_rank());
   const int per = TILE / S;  // S (a power of two <= 8) divides TILE
-  cluster_wait_acquire();  // every peer has started: its shared memory is live
+  if (tid == 0) mbar_arrive_expect_tx(&xbar, static_cast<uint32_t>(TILE * 4));  // S peers x per floats
+  cluster_wait_acquire();  // every peer has started: its shared memory and barrier are live
   for (int i = tid; i < TILE; i += WARPS * 32) {
     float s = 0.f;
 #pragma unroll
     for (int w = 0; w < WARPS; ++w) s += red[w][i];
     const int owner = i / per;
-    *cluster.map_shared_rank(part + me * per + (i - owner * per), owner) = s;
+    st_async_f32(cluster_addr(part + me * per + (i - owner * per), owner), s, cluster_addr(&xbar, owner));
   }
-  cluster_arrive_release();
-  cluster_wait_acquire();
+  const bool ok = mbar_wait_bounded(&xbar, 0, 1 << 21);
   const int ib = me * per, ie = ib + per;
   for (int i = ib + tid; i < ie; i += WARPS * 32) {
     float s = 0.f;
     for (int r = 0; r < S; ++r) s += part[r * per + (i - ib)];
     int e, t;
     frag_to_tile<NT>(i, e, t);
-    if (e0 + e < E && t0 + t < T) logits[static_cast<int64_t>(t0 + t) * E + e0 + e] = s;
+    if (e0 + e < E && t0 + t < T)
+      logits[static_cast<int64_t>(t0 + t) * E + e0 + e] = ok ? s : __int_as_float(0x7FC00000);
   }
 }
 

@@ -55,6 +55,7 @@ tail_kernel(const TailParams p) {
   __shared__ float w_s[MOE_MAX_K];
   __shared__ float red[33];
   __shared__ float cluster_slots[8 * (kMaxThreads / 32)];  // [cluster rank][warp]
+  __shared__ uint64_t ss_bar;  // split rows: completes when every CTA's warp sums have landed
 
   const int t = blockIdx.y;
   const int tid = threadIdx.x;
@@ -68,7 +69,13 @@ tail_kernel(const TailParams p) {
   const int64_t row_off = static_cast<int64_t>(t) * p.H;
   const int k = p.k;
 
-  if (cs > 1) cluster_arrive_relaxed();
+  if (cs > 1) {
+    if (tid == 0) {
+      mbar_init(&ss_bar, 1);
+      mbar_init_fence();  // visible to the cluster's remote stores after the cluster barrier below
+    }
+    cluster_arrive_relaxed();
+  }
   allow_dependent_launch();
   // While the previous kernel finishes: L2 prefetch of this CTA's slice of the
   // token's rows (hints only; the loads below come after the dependency wait
@@ -258,9 +265,14 @@ tail_kernel(const TailParams p) {
     }
   }
 
-  // sum of squares over the token's row: the block, then the cluster (one
-  // exchange of warp sums when the row is split over a cluster)
-  ss = cs > 1 ? cluster_block_sum(ss, cluster_slots) : block_sum(ss, red);
+  // sum of squares over the token's row: the block, or, when the row is split
+  // over a cluster, one exchange of warp sums by remote stores
+  if (cs > 1) {
+    if (!cluster_block_sum_async(ss, cluster_slots, &ss_bar) && tid == 0 && p.err_flag)
+      atomicOr(p.err_flag, MOE_FLAG_TIMEOUT);
+  } else {
+    ss = block_sum(ss, red);
+  }
   const float inv = rsqrtf(ss / static_cast<float>(p.H) + p.eps);
 
   // -- RMSNorm output
