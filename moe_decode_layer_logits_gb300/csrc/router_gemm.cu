@@ -4,8 +4,13 @@
 //
 // At decode sizes (T <= 64) the 3 MB gate weight is the whole cost, so the
 // kernel is organised to stream W once across as many SMs as possible:
-//  - a CTA owns 16 experts x (8*NT) tokens and a slice of the hidden dimension;
-//    its warps split that slice again;
+//  - a CTA owns 16*MT experts x 8*NT tokens and a slice of the hidden
+//    dimension; its warps split that slice again.  Up to 8 tokens: 32-expert
+//    tiles (half as many CTAs, each gate-weight fragment staged once per CTA);
+//    up to 64 tokens: 16-expert x 16-token tiles;
+//  - the first round of each lane's gate-weight fragments is copied into
+//    shared memory (cp.async) before the dependency wait: W is a model
+//    parameter, so only x waits for the previous kernel;
 //  - the CTAs that share an (expert, token) tile form a thread-block cluster
 //    (split-K over H) and add their partial tiles through distributed shared
 //    memory (remote stores counted on the owner's mbarrier) in ascending rank
@@ -23,7 +28,9 @@
 
 namespace moe {
 
-constexpr int kRouterUnroll = 4;
+constexpr size_t kRouterStaticSmem = 48 * 1024;  // larger router CTAs take dynamic shared memory
+
+
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -35,13 +42,14 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 }
 
 // Partial tiles are kept in accumulator-fragment order: element
-// i = (nt * 4 + reg) * 32 + lane holds expert g + 8 * (reg >> 1) and token
-// 8 * nt + 2 * q + (reg & 1) of the tile (g = lane / 4, q = lane % 4), so
-// that every shared-memory access below is conflict-free.
-template <int NT>
+// i = ((mt * NT + nt) * 4 + reg) * 32 + lane holds expert 16 mt + g +
+// 8 (reg >> 1) and token 8 nt + 2 q + (reg & 1) of the tile (g = lane / 4,
+// q = lane % 4), so that every shared-memory access below is conflict-free.
+template <int NT, int MT>
 __device__ __forceinline__ void frag_to_tile(int i, int& e, int& t) {
-  const int lane = i & 31, reg = (i >> 5) & 3, nt = i >> 7;
-  e = (lane >> 2) + 8 * (reg >> 1);
+  const int lane = i & 31, reg = (i >> 5) & 3, f = i >> 7;
+  const int nt = f % NT, mt = f / NT;
+  e = 16 * mt + (lane >> 2) + 8 * (reg >> 1);
   t = 8 * nt + 2 * (lane & 3) + (reg & 1);
 }
 
@@ -55,21 +63,29 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool full
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-template <int NT, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32)
-router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, float* __restrict__ logits,
-              int T, int H, int E) {
-  constexpr int TILE = 16 * 8 * NT;  // outputs per tile
-  __shared__ float red[WARPS][TILE];
-  __shared__ float part[TILE];  // S > 1: part[src * per + i] = rank src's partial of output ib + i
+// Shared memory of one router CTA (16 MT experts x 8 NT tokens, WARPS warps,
+// U 32-wide chunks of H per warp and round).
+template <int NT, int WARPS, int MT, int U>
+struct RouterSmem {
+  static constexpr int kTile = 16 * MT * 8 * NT;  // outputs per tile
   // each lane's gate-weight fragments of its warp's first round, staged before
   // the dependency wait (every thread reads back only its own slots)
-  __shared__ uint4 w_stage[WARPS][kRouterUnroll][2][32];
-  __shared__ uint64_t xbar;  // S > 1: completes when every CTA's partials of this CTA's outputs have landed
+  uint4 w_stage[WARPS][U][MT][2][32];
+  float red[WARPS][kTile];
+  float part[kTile];  // split-K: part[src * per + i] = rank src's partial of output ib + i
+  uint64_t xbar;      // split-K: completes when every CTA's partials of this CTA's outputs have landed
+};
+
+template <int NT, int WARPS, int MT, int U>
+__device__ __forceinline__ void router_body(RouterSmem<NT, WARPS, MT, U>& sm, const uint16_t* __restrict__ x,
+                                            const uint16_t* __restrict__ W, float* __restrict__ logits, int T,
+                                            int H, int E) {
+  constexpr int TILE = RouterSmem<NT, WARPS, MT, U>::kTile;
+  constexpr int kRouterUnroll = U;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
-  const int e0 = blockIdx.x * 16, t0 = blockIdx.y * 8 * NT;
+  const int e0 = blockIdx.x * 16 * MT, t0 = blockIdx.y * 8 * NT;
   const int S = gridDim.z, z = blockIdx.z;
   const int C = (H + 31) >> 5;
   const int cb = static_cast<int>(static_cast<int64_t>(C) * z / S);
@@ -79,7 +95,7 @@ router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, fl
 
   if (S > 1) {
     if (tid == 0) {
-      mbar_init(&xbar, 1);
+      mbar_init(&sm.xbar, 1);
       mbar_init_fence();  // visible to the cluster's remote stores after the cluster barrier
     }
     cluster_arrive_relaxed();
@@ -91,15 +107,22 @@ router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, fl
   // whatever the hint fetched).
   if (ce > cb) {
     const int h0 = cb * 32, h1 = min(H, ce * 32);
-    if (tid < 16 && e0 + tid < E)
+    if (tid < 16 * MT && e0 + tid < E)
       prefetch_l2(W + static_cast<int64_t>(e0 + tid) * H + h0, static_cast<uint32_t>((h1 - h0) * 2));
-    else if (blockIdx.x == 0 && tid >= 32 && tid < 32 + 8 * NT && t0 + tid - 32 < T)  // once per slice of x
-      prefetch_l2(x + static_cast<int64_t>(t0 + tid - 32) * H + h0, static_cast<uint32_t>((h1 - h0) * 2));
+    else if (blockIdx.x == 0 && tid >= 32 * MT && tid < 32 * MT + 8 * NT && t0 + tid - 32 * MT < T)
+      prefetch_l2(x + static_cast<int64_t>(t0 + tid - 32 * MT) * H + h0, static_cast<uint32_t>((h1 - h0) * 2));
   }
-  const int eA = e0 + g, eB = e0 + g + 8;
-  const bool okA = eA < E, okB = eB < E;
-  const uint16_t* pA = W + static_cast<int64_t>(okA ? eA : 0) * H + 8 * q;
-  const uint16_t* pB = W + static_cast<int64_t>(okB ? eB : 0) * H + 8 * q;
+  // this lane's gate-weight rows: expert 16 mt + g (A) and 16 mt + g + 8 (B)
+  const uint16_t* pw[MT][2];
+  bool okw[MT][2];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = e0 + 16 * mt + g + 8 * h;
+      okw[mt][h] = e < E;
+      pw[mt][h] = W + static_cast<int64_t>(okw[mt][h] ? e : 0) * H + 8 * q;
+    }
   // The gate weight is a model parameter that no kernel still running on the
   // stream writes, so its first round is copied into shared memory while the
   // previous kernel finishes; only x is read after the dependency wait.
@@ -109,8 +132,12 @@ router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, fl
     const int cc = wb + u;
     const bool ok = cc < we && (cc * 32 + 8 * q) < H;
     const int64_t off = static_cast<int64_t>(cc) * 32;
-    cp_async16(&w_stage[warp][u][0][lane], (ok && okA) ? static_cast<const void*>(pA + off) : W, ok && okA);
-    cp_async16(&w_stage[warp][u][1][lane], (ok && okB) ? static_cast<const void*>(pB + off) : W, ok && okB);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        cp_async16(&sm.w_stage[warp][u][mt][h][lane],
+                   (ok && okw[mt][h]) ? static_cast<const void*>(pw[mt][h] + off) : W, ok && okw[mt][h]);
   }
   cp_async_commit();
   grid_dependency_wait();
@@ -123,9 +150,11 @@ router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, fl
     px[nt] = x + static_cast<int64_t>(okx[nt] ? tt : 0) * H + 8 * q;
   }
 
-  float acc[NT][4];
+  float acc[MT][NT][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
 
   const uint4 zero = make_uint4(0, 0, 0, 0);
   // one round: kRouterUnroll 32-wide chunks of H starting at chunk c
@@ -139,53 +168,56 @@ router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, fl
       for (int nt = 0; nt < NT; ++nt) b[u][nt] = (ok && okx[nt]) ? ld_keep16(px[nt] + off) : zero;
     }
   };
-  auto mma_round = [&](const uint4 (&a)[kRouterUnroll][2], const uint4 (&b)[kRouterUnroll][NT]) {
+  auto mma_chunk = [&](int mt, const uint4& a0, const uint4& a1, const uint4 (&b)[NT]) {
 #pragma unroll
-    for (int u = 0; u < kRouterUnroll; ++u) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        mma_bf16_16816(acc[nt], a[u][0].x, a[u][1].x, a[u][0].y, a[u][1].y, b[u][nt].x, b[u][nt].y);
-        mma_bf16_16816(acc[nt], a[u][0].z, a[u][1].z, a[u][0].w, a[u][1].w, b[u][nt].z, b[u][nt].w);
-      }
+    for (int nt = 0; nt < NT; ++nt) {
+      mma_bf16_16816(acc[mt][nt], a0.x, a1.x, a0.y, a1.y, b[nt].x, b[nt].y);
+      mma_bf16_16816(acc[mt][nt], a0.z, a1.z, a0.w, a1.w, b[nt].z, b[nt].w);
     }
   };
   {  // first round: the gate weight from the fragments staged before the wait
-    uint4 a[kRouterUnroll][2], b[kRouterUnroll][NT];
+    uint4 b[kRouterUnroll][NT];
     load_x(wb, b);
     cp_async_wait_all();  // this thread's own staged fragments
 #pragma unroll
-    for (int u = 0; u < kRouterUnroll; ++u) {
-      a[u][0] = w_stage[warp][u][0][lane];
-      a[u][1] = w_stage[warp][u][1][lane];
-    }
-    mma_round(a, b);
+    for (int u = 0; u < kRouterUnroll; ++u)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+        mma_chunk(mt, sm.w_stage[warp][u][mt][0][lane], sm.w_stage[warp][u][mt][1][lane], b[u]);
   }
   for (int c = wb + kRouterUnroll; c < we; c += kRouterUnroll) {
-    uint4 a[kRouterUnroll][2], b[kRouterUnroll][NT];
+    uint4 a[kRouterUnroll][MT][2], b[kRouterUnroll][NT];
 #pragma unroll
     for (int u = 0; u < kRouterUnroll; ++u) {
       const int cc = c + u;
       const bool ok = cc < we && (cc * 32 + 8 * q) < H;
       const int64_t off = static_cast<int64_t>(cc) * 32;
-      a[u][0] = (ok && okA) ? ld_stream16(pA + off) : zero;
-      a[u][1] = (ok && okB) ? ld_stream16(pB + off) : zero;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) a[u][mt][h] = (ok && okw[mt][h]) ? ld_stream16(pw[mt][h] + off) : zero;
     }
     load_x(c, b);
-    mma_round(a, b);
+#pragma unroll
+    for (int u = 0; u < kRouterUnroll; ++u)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) mma_chunk(mt, a[u][mt][0], a[u][mt][1], b[u]);
   }
 
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int r = 0; r < 4; ++r) red[warp][(nt * 4 + r) * 32 + lane] = acc[nt][r];
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) sm.red[warp][((mt * NT + nt) * 4 + r) * 32 + lane] = acc[mt][nt][r];
   __syncthreads();
   if (S == 1) {
     for (int i = tid; i < TILE; i += WARPS * 32) {
       float s = 0.f;
 #pragma unroll
-      for (int w = 0; w < WARPS; ++w) s += red[w][i];
+      for (int w = 0; w < WARPS; ++w) s += sm.red[w][i];
       int e, t;
-      frag_to_tile<NT>(i, e, t);
+      frag_to_tile<NT, MT>(i, e, t);
       if (e0 + e < E && t0 + t < T) logits[static_cast<int64_t>(t0 + t) * E + e0 + e] = s;
     }
     return;
@@ -198,44 +230,73 @@ router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, fl
   cg::cluster_group cluster = cg::this_cluster();
   const int me = static_cast<int>(cluster.block_rank());
   const int per = TILE / S;  // S (a power of two <= 8) divides TILE
-  if (tid == 0) mbar_arrive_expect_tx(&xbar, static_cast<uint32_t>(TILE * 4));  // S peers x per floats
+  if (tid == 0) mbar_arrive_expect_tx(&sm.xbar, static_cast<uint32_t>(TILE * 4));  // S peers x per floats
   cluster_wait_acquire();  // every peer has started: its shared memory and barrier are live
   for (int i = tid; i < TILE; i += WARPS * 32) {
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < WARPS; ++w) s += red[w][i];
+    for (int w = 0; w < WARPS; ++w) s += sm.red[w][i];
     const int owner = i / per;
-    st_async_f32(cluster_addr(part + me * per + (i - owner * per), owner), s, cluster_addr(&xbar, owner));
+    st_async_f32(cluster_addr(sm.part + me * per + (i - owner * per), owner), s, cluster_addr(&sm.xbar, owner));
   }
-  const bool ok = mbar_wait_bounded(&xbar, 0, 1 << 21);
+  const bool ok = mbar_wait_bounded(&sm.xbar, 0, 1 << 21);
   const int ib = me * per, ie = ib + per;
   for (int i = ib + tid; i < ie; i += WARPS * 32) {
     float s = 0.f;
-    for (int r = 0; r < S; ++r) s += part[r * per + (i - ib)];
+    for (int r = 0; r < S; ++r) s += sm.part[r * per + (i - ib)];
     int e, t;
-    frag_to_tile<NT>(i, e, t);
+    frag_to_tile<NT, MT>(i, e, t);
     if (e0 + e < E && t0 + t < T)
       logits[static_cast<int64_t>(t0 + t) * E + e0 + e] = ok ? s : __int_as_float(0x7FC00000);
   }
 }
 
-// Decode sizes (T <= 64): tiles of 8 or 16 tokens, 8 warps splitting each
-// CTA's slice of H so that every warp loads its share in one round, and a
-// cluster of up to 8 CTAs along H.  Larger T: 32-token tiles, 4 warps.
-template <int NT, int WARPS>
+// The kernel: shared memory declared statically where it fits in 48 KB, else
+// taken from the dynamic allocation (opted in at launch).
+template <int NT, int WARPS, int MT, int U>
+__global__ void __launch_bounds__(WARPS * 32, (WARPS == 8 && MT == 1) ? 4 : 1)  // 16-token tiles: 4 CTAs an SM
+router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ W, float* __restrict__ logits,
+              int T, int H, int E) {
+  using Smem = RouterSmem<NT, WARPS, MT, U>;
+  if constexpr (sizeof(Smem) <= kRouterStaticSmem) {
+    __shared__ Smem sm;
+    router_body<NT, WARPS, MT, U>(sm, x, W, logits, T, H, E);
+  } else {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    router_body<NT, WARPS, MT, U>(*reinterpret_cast<Smem*>(smem_raw), x, W, logits, T, H, E);
+  }
+}
+
+// Decode sizes (T <= 64): tiles of 8 or 16 tokens and 16 MT experts, 8 warps
+// splitting each CTA's slice of H so that every warp loads its share in one
+// round, and a cluster of up to 8 CTAs along H.  Larger T (only with H < 64):
+// 32-token tiles, 4 warps.
+template <int NT, int WARPS, int MT, int U>
 static cudaError_t launch_router(const uint16_t* x, const uint16_t* W, float* logits, int T, int H, int E,
                                  int nsm, cudaStream_t stream) {
+  using Smem = RouterSmem<NT, WARPS, MT, U>;
+  constexpr bool kDynamic = sizeof(Smem) > kRouterStaticSmem;
+  static bool smem_opt_in[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (kDynamic && dev >= 0 && dev < 64 && !smem_opt_in[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(router_kernel<NT, WARPS, MT, U>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(sizeof(Smem)));
+    if (e != cudaSuccess) return e;
+    smem_opt_in[dev] = true;
+  }
   const int t_tiles = (T + 8 * NT - 1) / (8 * NT);
-  const int e_tiles = (E + 15) / 16;
+  const int e_tiles = (E + 16 * MT - 1) / (16 * MT);
   const int C = (H + 31) / 32;
   int S = 1;
-  // split H over a cluster until the grid covers every SM twice (or each
+  // split H over a cluster until the grid covers every SM four times (or each
   // warp would get fewer than one 32-wide chunk per slice)
   while (S < 8 && static_cast<int64_t>(e_tiles) * t_tiles * S < 4 * nsm && C / (2 * S) >= WARPS) S *= 2;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(e_tiles, t_tiles, S);
   cfg.blockDim = dim3(WARPS * 32, 1, 1);
-  cfg.dynamicSmemBytes = launch_smem(0);
+  cfg.dynamicSmemBytes = launch_smem(kDynamic ? sizeof(Smem) : 0);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0] = pdl_attribute();
@@ -248,7 +309,7 @@ static cudaError_t launch_router(const uint16_t* x, const uint16_t* W, float* lo
     cfg.numAttrs = 2;
   }
   cfg.attrs = attr;
-  return cudaLaunchKernelEx(&cfg, router_kernel<NT, WARPS>, x, W, logits, T, H, E);
+  return cudaLaunchKernelEx(&cfg, router_kernel<NT, WARPS, MT, U>, x, W, logits, T, H, E);
 }
 
 }  // namespace moe
@@ -291,9 +352,9 @@ extern "C" int moe_router_logits_fp32(const void* x_bf16, const void* w_gate_bf1
     float* lc = logits_out + t0 * E;
     const int Hi = static_cast<int>(H), Ei = static_cast<int>(E);
     cudaError_t e;
-    if (T > 64) e = launch_router<4, 4>(xc, W, lc, Tc, Hi, Ei, nsm, stream);
-    else if (NT == 1) e = launch_router<1, 8>(xc, W, lc, Tc, Hi, Ei, nsm, stream);
-    else e = launch_router<2, 8>(xc, W, lc, Tc, Hi, Ei, nsm, stream);
+    if (T > 64) e = launch_router<4, 4, 1, 4>(xc, W, lc, Tc, Hi, Ei, nsm, stream);
+    else if (NT == 1) e = launch_router<1, 8, 2, 3>(xc, W, lc, Tc, Hi, Ei, nsm, stream);
+    else e = launch_router<2, 8, 1, 4>(xc, W, lc, Tc, Hi, Ei, nsm, stream);
     if (e != cudaSuccess) {
       (void)cudaGetLastError();
       return MOE_ERR_CUDA;
