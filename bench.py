@@ -58,7 +58,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--min-timed-s", type=float, default=1.0,
                     help="repeat the K-step timed region until this much time is covered")
-    ap.add_argument("--ncu-case", choices=["decode", "prefill", "router"], default=None,
+    ap.add_argument("--ncu-case", choices=["decode", "decode1", "prefill", "router"], default=None,
                     help="run a small fixed case for an ncu capture and exit (no timing, no JSON)")
     return ap.parse_args()
 
@@ -851,7 +851,8 @@ def run_reference(args):
 def run_ncu_case(case):
     """Small cases for ncu captures (a few hundred MB, more than the L2):
     decode -- 12 layers at T=64 (162 MB), router -> route -> finalize -> fused
-    tail on each layer, twice; prefill -- 2 sets at T=2048 (605 MB), route, finalize and the
+    tail on each layer, twice; decode1 -- the same with 48 layers at T=1
+    (154 MB, mostly gate weights); prefill -- 2 sets at T=2048 (605 MB), route, finalize and the
     router-less fused tail on each set, twice; router -- the router GEMM on 2
     inputs at T=8192 (x 100 MB each), twice."""
     import torch
@@ -869,18 +870,20 @@ def run_ncu_case(case):
         return
     if case == "decode":
         sets = [device_layer(T_DEC, H_DEC, E_DEC, K_DEC, seed=i, scale=SCALE) for i in range(12)]
+    elif case == "decode1":
+        sets = [device_layer(1, H_DEC, E_DEC, K_DEC, seed=i, scale=SCALE) for i in range(48)]
     else:
         sets = [device_layer(2048, H_DEC, E_DEC, K_DEC, seed=100 + i, scale=SCALE, router=False, logits=True)
                 for i in range(2)]
     torch.cuda.synchronize()
     for _ in range(2):
         for d in sets:
-            if case == "decode":
+            if case in ("decode", "decode1"):
                 M.moe_router_logits_fp32(d["x"], d["w_gate"], logits_out=d["logits"])
             M.moe_topk_route(d["logits"], K_DEC, SCALE, topk_ids=d["topk_ids"], topk_w=d["topk_w"])
             M.moe_finalize_add_rmsnorm(d["rows"], d["map"], d["topk_w"], d["shared"], d["residual"], d["gamma"],
                                        d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"])
-            if case == "decode":
+            if case in ("decode", "decode1"):
                 M.moe_tail_fused(d["logits"], K_DEC, SCALE, d["rows"], d["map"], d["shared"], d["residual"],
                                  d["gamma"], d["eps"], residual_out=d["residual_out"], normed_out=d["normed_out"],
                                  topk_ids=d["topk_ids"], topk_w=d["topk_w"])

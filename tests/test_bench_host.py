@@ -78,3 +78,8 @@ def test_committed_profiles_are_complete():
         for f in info["source_files"].split():
             assert os.path.exists(os.path.join(ROOT, f)), (n, f)
         assert re.fullmatch(r"[0-9a-f]{16}", info["source_sha256"]), n
+        # the counters were taken on the sources as they are now: bench.py
+        # can quote them as the roofline traffic (a stale digest reads None)
+        units = int(info["units_per_launch"])
+        assert bench.ncu_traffic(n[:-3], units) == pytest.approx(int(info["dram_bytes_per_launch"])), (
+            n, "stale: a listed source changed after the capture")
