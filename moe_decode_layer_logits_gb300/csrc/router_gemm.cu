@@ -5,9 +5,9 @@
 // At decode sizes (T <= 64) the 3 MB gate weight is the whole cost, so the
 // kernel is organised to stream W once across as many SMs as possible:
 //  - a CTA owns 16*MT experts x 8*NT tokens and a slice of the hidden
-//    dimension; its warps split that slice again.  Up to 8 tokens: 32-expert
-//    tiles (half as many CTAs, each gate-weight fragment staged once per CTA);
-//    up to 64 tokens: 16-expert x 16-token tiles;
+//    dimension; its warps split that slice again.  Up to 32 tokens: 32-expert
+//    tiles of 8 or 16 tokens (half as many CTAs, each gate-weight fragment
+//    staged once per CTA); up to 64 tokens: 16-expert x 16-token tiles;
 //  - the first round of each lane's gate-weight fragments is copied into
 //    shared memory (cp.async) before the dependency wait: W is a model
 //    parameter, so only x waits for the previous kernel;
@@ -354,6 +354,7 @@ extern "C" int moe_router_logits_fp32(const void* x_bf16, const void* w_gate_bf1
     cudaError_t e;
     if (T > 64) e = launch_router<4, 4, 1, 4>(xc, W, lc, Tc, Hi, Ei, nsm, stream);
     else if (NT == 1) e = launch_router<1, 8, 2, 3>(xc, W, lc, Tc, Hi, Ei, nsm, stream);
+    else if (T <= 32) e = launch_router<2, 8, 2, 3>(xc, W, lc, Tc, Hi, Ei, nsm, stream);
     else e = launch_router<2, 8, 1, 4>(xc, W, lc, Tc, Hi, Ei, nsm, stream);
     if (e != cudaSuccess) {
       (void)cudaGetLastError();

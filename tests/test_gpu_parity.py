@@ -61,6 +61,9 @@ ROUTER = [  # (T, H, E)
     (256, 6144, 256), (300, 2048, 64), (513, 6144, 256), (8192, 512, 256),
     (384, 6144, 256), (512, 6144, 256), (768, 6144, 256), (2000, 6144, 168), (2048, 6144, 256),
     (4000, 6144, 256), (65, 6144, 256), (130, 6144, 168), (200, 6144, 256),
+    # up to 32 tokens the decode router takes 32-expert tiles: full and partial
+    # token and expert tiles
+    (20, 6144, 256), (32, 2048, 168), (17, 1024, 40), (29, 2056, 72),
 ]
 
 
