@@ -88,7 +88,7 @@ const char* moe_status_string(int status);
  * call is made (x may be: it is read only after that wait).
  *
  * Batches of more than 64 tokens (H >= 64) run a pipelined tensor-memory
- * kernel whose waits are bounded (about two seconds each); if one runs out,
+ * kernel whose waits are bounded (2^21 probes, seconds at most); if one runs out,
  * the logits of that launch's affected 128-expert x token tiles are written
  * as NaN (a quiet NaN in every element of the tile) and the call still
  * returns MOE_OK, as the launch was made.  NaN logits then give unspecified
@@ -175,7 +175,7 @@ int moe_tail_fused(const float* logits, int64_t E, int32_t k, float routed_scale
  * launch of the persistent tail kernel (the path taken by batches of at
  * least two tokens per SM) leaves stage `stage` of its first CTA unarmed and
  * uncopied, so that CTA's consumers wait for it until their bounded wait
- * runs out (about two seconds), set MOE_FLAG_TIMEOUT in err_flag and stop
+ * runs out (2^21 probes, seconds at most), set MOE_FLAG_TIMEOUT in err_flag and stop
  * waiting; the launch still completes, its outputs are invalid, and the next
  * launch is unaffected.  One launch takes the request (a decode-size launch
  * leaves it for the next persistent one); stage -1 cancels it.  Returns

@@ -138,16 +138,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// One probe of phase `parity`; the hardware may suspend the thread for up to
-// about `hint_ns` before it reports "not yet".
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+// One probe of phase `parity`.  It carries no suspend-time hint: with a 1 us
+// hint, waits on stage rings and exchanges came back measurably later (the
+// tcgen05 router's stage ring: +1.4 us on a 128-CTA launch at T = 8192; the
+// persistent tail at T = 512: +0.18 us; the decode layer: +0.05 us).
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "r"(smem_addr(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -168,11 +170,11 @@ __device__ __forceinline__ void st_async_f32(uint32_t remote, float v, uint32_t 
                : "memory");
 }
 
-// Probes of phase `parity` of `bar` until it completes; false after about
-// `max_probes` probes of up to 1 us each.
+// Probes of phase `parity` of `bar` until it completes; false after
+// `max_probes` probes.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int max_probes) {
   for (int it = 0; it < max_probes; ++it)
-    if (mbar_try_wait(bar, parity, 1000)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
 

@@ -167,23 +167,9 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]
 
 // Bounded wait; gives up early once the CTA's abort flag is raised unless
 // `drain` is set (a drain must see the phase, abort or not).
-// The try_wait carries no suspend-time hint: with a 1 us hint the waits on
-// the stage ring added 1.4 us to a 128-CTA launch at T = 8192.
-__device__ __forceinline__ bool tc_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, bool drain) {
   for (int it = 0; it < kTcMaxWaits; ++it) {
-    if (tc_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (!drain && *abort_flag) return false;
   }
   *abort_flag = 1;

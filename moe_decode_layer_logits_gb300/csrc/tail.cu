@@ -327,8 +327,7 @@ constexpr int kMaxAhead = 4;  // tokens whose rows the producer requests into th
 constexpr int kLogitsAhead = 3;  // router-less tail: logits rows requested into the L2 this many tokens ahead
 constexpr int kWRing = 4;
 constexpr int kStreamSmemBudget = 200 * 1024;
-constexpr uint32_t kProbeHintNs = 1000;
-constexpr int kMaxProbes = 1 << 21;  // ~2 s of probes per wait before giving up
+constexpr int kMaxProbes = 1 << 21;  // probes per wait before giving up
 
 struct StreamShape {
   int chunk;        // row elements per stage (multiple of 8)
@@ -343,7 +342,7 @@ struct StreamShape {
 __device__ __forceinline__ bool stream_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                             int32_t* err_flag) {
   for (int it = 0; it < kMaxProbes; ++it) {
-    if (mbar_try_wait(bar, parity, kProbeHintNs)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
   }
   *abort_flag = 1;
@@ -533,7 +532,7 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
       for (int u = issued > sh.nstages ? issued - sh.nstages : 0; u < issued; ++u) {
         if (u == withheld) continue;
         for (int it = 0; it < kMaxProbes; ++it)
-          if (mbar_try_wait(&full_bar[u % sh.nstages], (u / sh.nstages) & 1, kProbeHintNs)) break;
+          if (mbar_try_wait(&full_bar[u % sh.nstages], (u / sh.nstages) & 1)) break;
       }
     }
   } else if (warp == 1) {
