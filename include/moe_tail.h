@@ -77,6 +77,8 @@ const char* moe_status_string(int status);
  *   x_bf16      [T, H]  BF16, 16-byte aligned
  *   w_gate_bf16 [E, H]  BF16, 16-byte aligned
  *   logits_out  [T, E]  FP32, written
+ *   err_flag    device int32 or NULL: MOE_FLAG_TIMEOUT is OR-ed into it when
+ *               a bounded wait of the tensor-memory kernel runs out (below)
  *   T >= 0; H >= 8, H % 8 == 0; 1 <= E <= MOE_MAX_E.
  *
  * Products are exact; partial sums are FP32 (tensor-core accumulate), so
@@ -87,16 +89,18 @@ const char* moe_status_string(int status);
  * not be written by a kernel that may still be running on `stream` when this
  * call is made (x may be: it is read only after that wait).
  *
- * Batches of more than 64 tokens (H >= 64) run a pipelined tensor-memory
- * kernel whose waits are bounded (2^21 probes, seconds at most); if one runs out,
- * the logits of that launch's affected 128-expert x token tiles are written
- * as NaN (a quiet NaN in every element of the tile) and the call still
- * returns MOE_OK, as the launch was made.  NaN logits then give unspecified
- * ids downstream; a caller that must tell them from bad inputs checks the
- * logits for NaN.
+ * Every wait inside the kernels is bounded (2^21 probes, seconds at most):
+ * the split-K exchange of the decode-size kernel and the stage pipeline of
+ * the tensor-memory kernel that batches of more than 64 tokens (H >= 64)
+ * take.  If one runs out, the logits of the affected tile (a split-K owner's
+ * outputs, or a 128-expert x token tile) are written as NaN (a quiet NaN in
+ * every element) and the call still returns MOE_OK, as the launch was made;
+ * the tensor-memory kernel also OR-s MOE_FLAG_TIMEOUT into *err_flag (if
+ * err_flag is given), the decode-size kernel reports it in the logits only.
+ * NaN logits give unspecified ids downstream.
  */
 int moe_router_logits_fp32(const void* x_bf16, const void* w_gate_bf16, float* logits_out,
-                           int64_t T, int64_t H, int64_t E, cudaStream_t stream);
+                           int64_t T, int64_t H, int64_t E, int32_t* err_flag, cudaStream_t stream);
 
 /*
  * Top-k routing: per token the k largest logits (descending; equal logits in
@@ -182,6 +186,18 @@ int moe_tail_fused(const float* logits, int64_t E, int32_t k, float routed_scale
  * MOE_OK, or MOE_ERR_INVALID_ARG for stage < -1.  Not for production use.
  */
 int moe_debug_withhold_stream_stage(int32_t stage);
+
+/*
+ * Test hook of the router's bounded waits; no counterpart on the pages.  The
+ * next launch of the tensor-memory router kernel (batches of more than 64
+ * tokens, H >= 64) issues no loads for K block `kb` (64 columns of H) in its
+ * first CTA, so that CTA's MMA warp waits for them until its bounded wait
+ * runs out: the first 128-expert x token tile is written as NaN and
+ * MOE_FLAG_TIMEOUT is set in err_flag; the other tiles are correct and the
+ * next launch is unaffected.  kb -1 cancels the request.  Returns MOE_OK, or
+ * MOE_ERR_INVALID_ARG for kb < -1.  Not for production use.
+ */
+int moe_debug_withhold_router_stage(int32_t kb);
 
 /*
  * Test hook of the launch-error path; no counterpart on the pages.  With

@@ -23,6 +23,7 @@ from ._lib import MoeTailError, check, lib
 
 __all__ = [
     "moe_debug_withhold_stream_stage",
+    "moe_debug_withhold_router_stage",
     "moe_debug_fail_next_launch",
     "moe_debug_router_tc_shape",
     "moe_router_logits_fp32",
@@ -58,14 +59,18 @@ def _ptr(t, dtype, name, ndim=None, optional=False):
     return t.data_ptr()
 
 
-def moe_router_logits_fp32(x, w_gate, logits_out=None, stream=None):
-    """logits[T, E] = x[T, H] . w_gate[E, H]^T (BF16 in, FP32 accumulate and out)."""
+def moe_router_logits_fp32(x, w_gate, logits_out=None, err_flag=None, stream=None):
+    """logits[T, E] = x[T, H] . w_gate[E, H]^T (BF16 in, FP32 accumulate and out).
+    err_flag: optional int32 CUDA tensor; MOE_FLAG_TIMEOUT is OR-ed into it
+    when a bounded wait of the tensor-memory kernel (T > 64) runs out (the
+    affected logits are NaN either way)."""
     T, H = x.shape
     E = w_gate.shape[0]
     if logits_out is None:
         logits_out = torch.empty((T, E), dtype=torch.float32, device=x.device)
     st = lib().moe_router_logits_fp32(_ptr(x, torch.bfloat16, "x", 2), _ptr(w_gate, torch.bfloat16, "w_gate", 2),
-                                      _ptr(logits_out, torch.float32, "logits_out", 2), T, H, E, _stream(stream))
+                                      _ptr(logits_out, torch.float32, "logits_out", 2), T, H, E,
+                                      _ptr(err_flag, torch.int32, "err_flag", optional=True), _stream(stream))
     check(st, "moe_router_logits_fp32")
     return logits_out
 
@@ -141,6 +146,14 @@ def moe_debug_withhold_stream_stage(stage):
     leaves stage `stage` of its first CTA uncopied, so that CTA's wait runs
     out and MOE_FLAG_TIMEOUT is set; -1 cancels the request."""
     check(lib().moe_debug_withhold_stream_stage(int(stage)), "moe_debug_withhold_stream_stage")
+
+
+def moe_debug_withhold_router_stage(kb):
+    """Test hook of the router's bounded waits: the next tensor-memory router
+    launch issues no loads for K block `kb` in its first CTA, so that CTA's
+    wait runs out, its tile is written as NaN and MOE_FLAG_TIMEOUT is set;
+    -1 cancels the request."""
+    check(lib().moe_debug_withhold_router_stage(int(kb)), "moe_debug_withhold_router_stage")
 
 
 def moe_debug_fail_next_launch(on=True):

@@ -30,13 +30,14 @@ _f32 = ctypes.c_float
 
 SIGNATURES = {
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
-    "moe_router_logits_fp32": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "moe_router_logits_fp32": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
     "moe_topk_route": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i32, _f32, _vp]),
     "moe_finalize_add_rmsnorm": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _vp, _vp, _i32, _vp, _vp, _f32,
                                                 _vp, _vp, _i64, _i64, _vp, _vp]),
     "moe_tail_fused": (ctypes.c_int, [_vp, _i64, _i32, _f32, _vp, _i64, _vp, _vp, _vp, _vp, _f32, _vp, _vp,
                                       _vp, _vp, _i64, _i64, _vp, _vp]),
     "moe_debug_withhold_stream_stage": (ctypes.c_int, [_i32]),
+    "moe_debug_withhold_router_stage": (ctypes.c_int, [_i32]),
     "moe_debug_fail_next_launch": (ctypes.c_int, [_i32]),
     "moe_debug_router_tc_shape": (ctypes.c_int, [_i64, _i64, _i64, _i32, _i32, _i32, _i32, _vp, _vp]),
 }

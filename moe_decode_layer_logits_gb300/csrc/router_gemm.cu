@@ -314,14 +314,18 @@ static cudaError_t launch_router(const uint16_t* x, const uint16_t* W, float* lo
 
 }  // namespace moe
 
+// err_flag is raised by the tensor-memory kernel (T > 64); the decode-size
+// kernel marks a timed-out split-K exchange in its logits (NaN) only: a flag
+// store there, even one never executed, cost the decode layer about 0.05 us.
 extern "C" int moe_router_logits_fp32(const void* x_bf16, const void* w_gate_bf16, float* logits_out,
-                                      int64_t T, int64_t H, int64_t E, cudaStream_t stream) {
+                                      int64_t T, int64_t H, int64_t E, int32_t* err_flag, cudaStream_t stream) {
   using namespace moe;
   if (T < 0 || H < 8 || E < 1) return MOE_ERR_INVALID_ARG;
   if (H % 8 != 0 || E > MOE_MAX_E || H > (1 << 20)) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   if (!x_bf16 || !w_gate_bf16 || !logits_out) return MOE_ERR_INVALID_ARG;
-  if (!aligned(x_bf16, 16) || !aligned(w_gate_bf16, 16) || !aligned(logits_out, 4)) return MOE_ERR_MISALIGNED;
+  if (!aligned(x_bf16, 16) || !aligned(w_gate_bf16, 16) || !aligned(logits_out, 4) || (err_flag && !aligned(err_flag, 4)))
+    return MOE_ERR_MISALIGNED;
   const int nsm = sm_count();
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
   const uint16_t* W = static_cast<const uint16_t*>(w_gate_bf16);
@@ -331,7 +335,7 @@ extern "C" int moe_router_logits_fp32(const void* x_bf16, const void* w_gate_bf1
     for (int64_t t0 = 0; t0 < T; t0 += per) {
       const int Tc = static_cast<int>(T - t0 < per ? T - t0 : per);
       const cudaError_t e = launch_router_tc(x + t0 * H, W, logits_out + t0 * E, Tc, static_cast<int>(H),
-                                             static_cast<int>(E), nsm, stream);
+                                             static_cast<int>(E), err_flag, nsm, stream);
       if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return MOE_ERR_CUDA;

@@ -21,7 +21,8 @@
 //    writes are free of bank conflicts; the rows then leave as 16-byte
 //    stores, 512 contiguous bytes per warp.
 // Every wait is bounded; a tile whose pipeline gave up is written as NaN so
-// that the failure is visible in the output.
+// that the failure is visible in the output, and MOE_FLAG_TIMEOUT is raised
+// in the caller's error flag if one is given.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -176,10 +177,12 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile
   return false;
 }
 
+// withhold_kb (test hook): the K block whose loads the first CTA never
+// issues, so that its MMA warp's wait runs out; -1 in normal launches.
 template <int BNT>
 __global__ void __launch_bounds__(kTcThreads, 1)
 router_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
-                 float* __restrict__ logits, int T, int H, int E) {
+                 float* __restrict__ logits, int T, int H, int E, int32_t* err_flag, int withhold_kb) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem<BNT>& sm = *reinterpret_cast<TcSmem<BNT>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                     ~static_cast<uintptr_t>(1023));
@@ -214,18 +217,20 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
+      const int withheld = (blockIdx.x | blockIdx.y | blockIdx.z) == 0 ? withhold_kb : -1;
       int issued = 0;
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = kb % kTcStages, n = kb / kTcStages;
         if (n > 0 && !tc_wait(&sm.empty[s], (n - 1) & 1, abort_v, false)) break;
+        issued = kb + 1;
+        if (kb == withheld) continue;  // neither armed nor loaded: the MMA warp's wait runs out
         mbar_arrive_expect_tx(&sm.full[s], static_cast<uint32_t>((kTcBM + BNT) * kTcBK * 2));
         tma_load_2d(sm.a[s], &tmap_w, (kb0 + kb) * kTcBK, e0, &sm.full[s]);
         tma_load_2d(sm.b[s], &tmap_x, (kb0 + kb) * kTcBK, t0, &sm.full[s]);
-        issued = kb + 1;
       }
       // drain: no copy may land after this CTA exits
       for (int kb = issued > kTcStages ? issued - kTcStages : 0; kb < issued; ++kb)
-        tc_wait(&sm.full[kb % kTcStages], (kb / kTcStages) & 1, abort_v, true);
+        if (kb != withheld) tc_wait(&sm.full[kb % kTcStages], (kb / kTcStages) & 1, abort_v, true);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
@@ -330,6 +335,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
   }
   tc_fence_before_sync();
   __syncthreads();
+  if (threadIdx.x == 0 && err_flag && *abort_v) atomicOr(err_flag, MOE_FLAG_TIMEOUT);
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_d, tmem_cols(BNT));
@@ -418,7 +424,7 @@ static int tc_max_clusters(int dev, int S) {
 
 template <int BNT>
 static cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw, float* logits, int T, int H, int E,
-                             int S, int dev, cudaStream_t stream) {
+                             int32_t* err_flag, int withhold_kb, int S, int dev, cudaStream_t stream) {
   const cudaError_t oe = tc_opt_in<BNT>(dev);
   if (oe != cudaSuccess) return oe;
   cudaLaunchConfig_t cfg = {};
@@ -437,7 +443,7 @@ static cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw, float
     cfg.numAttrs = 2;
   }
   cfg.attrs = attr;
-  return cudaLaunchKernelEx(&cfg, router_tc_kernel<BNT>, mx, mw, logits, T, H, E);
+  return cudaLaunchKernelEx(&cfg, router_tc_kernel<BNT>, mx, mw, logits, T, H, E, err_flag, withhold_kb);
 }
 
 static int max_clusters_for(int bnt, int dev, int S) {
@@ -488,30 +494,41 @@ static TcShape choose_shape(int T, int H, int E, int nsm, MaxClusters max_cluste
 }
 
 template <int BNT>
-static cudaError_t launch_bnt(const void* x, const void* w, float* logits, int T, int H, int E, int S, int dev,
-                              cudaStream_t stream) {
+static cudaError_t launch_bnt(const void* x, const void* w, float* logits, int T, int H, int E, int32_t* err_flag,
+                              int withhold_kb, int S, int dev, cudaStream_t stream) {
   CUtensorMap mx, mw;
   if (!make_map(&mx, x, T, H, BNT) || !make_map(&mw, w, E, H, kTcBM)) return cudaErrorInvalidValue;
-  return launch_tc<BNT>(mx, mw, logits, T, H, E, S, dev, stream);
+  return launch_tc<BNT>(mx, mw, logits, T, H, E, err_flag, withhold_kb, S, dev, stream);
 }
 
-cudaError_t launch_router_tc(const void* x, const void* w, float* logits, int T, int H, int E, int nsm,
-                             cudaStream_t stream) {
+// Test hook of the bounded waits (moe_debug_withhold_router_stage): a K block
+// that the next tensor-memory router launch withholds, taken by that launch.
+static std::atomic<int> g_withheld_kb{-1};
+
+cudaError_t launch_router_tc(const void* x, const void* w, float* logits, int T, int H, int E, int32_t* err_flag,
+                             int nsm, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
   const TcShape sh = choose_shape(T, H, E, nsm, [dev](int bnt, int S) { return max_clusters_for(bnt, dev, S); });
+  const int wk = g_withheld_kb.exchange(-1);
   switch (sh.bnt) {
-    case 64: return launch_bnt<64>(x, w, logits, T, H, E, sh.S, dev, stream);
-    case 80: return launch_bnt<80>(x, w, logits, T, H, E, sh.S, dev, stream);
-    case 96: return launch_bnt<96>(x, w, logits, T, H, E, sh.S, dev, stream);
-    case 112: return launch_bnt<112>(x, w, logits, T, H, E, sh.S, dev, stream);
-    default: return launch_bnt<128>(x, w, logits, T, H, E, sh.S, dev, stream);
+    case 64: return launch_bnt<64>(x, w, logits, T, H, E, err_flag, wk, sh.S, dev, stream);
+    case 80: return launch_bnt<80>(x, w, logits, T, H, E, err_flag, wk, sh.S, dev, stream);
+    case 96: return launch_bnt<96>(x, w, logits, T, H, E, err_flag, wk, sh.S, dev, stream);
+    case 112: return launch_bnt<112>(x, w, logits, T, H, E, err_flag, wk, sh.S, dev, stream);
+    default: return launch_bnt<128>(x, w, logits, T, H, E, err_flag, wk, sh.S, dev, stream);
   }
 }
 
 bool router_tc_supported(int64_t T, int64_t H) { return T >= kRouterTcMinT && H >= kTcBK; }
 
 }  // namespace moe
+
+extern "C" int moe_debug_withhold_router_stage(int32_t kb) {
+  if (kb < -1) return MOE_ERR_INVALID_ARG;
+  moe::g_withheld_kb.store(kb);
+  return MOE_OK;
+}
 
 // Host-only test hook: the launch shape the tcgen05 router would take for a
 // device with `nsm` SMs that holds mc2 / mc4 / mc8 clusters of 2 / 4 / 8 CTAs

@@ -15,8 +15,9 @@ constexpr int64_t kRouterTcMinT = 65;
 
 bool router_tc_supported(int64_t T, int64_t H);
 
-// logits[T, E] = x[T, H] . W[E, H]^T on the tcgen05 tensor cores (one launch).
-cudaError_t launch_router_tc(const void* x, const void* w, float* logits, int T, int H, int E, int nsm,
-                             cudaStream_t stream);
+// logits[T, E] = x[T, H] . W[E, H]^T on the tcgen05 tensor cores (one launch);
+// a bounded wait that runs out raises MOE_FLAG_TIMEOUT in err_flag (if given).
+cudaError_t launch_router_tc(const void* x, const void* w, float* logits, int T, int H, int E, int32_t* err_flag,
+                             int nsm, cudaStream_t stream);
 
 }  // namespace moe

@@ -64,21 +64,22 @@ def test_status_strings(lib):
     assert "unknown" in L.status_string(99)
 
 
-# -- moe_router_logits_fp32(x, w, logits, T, H, E, stream)
+# -- moe_router_logits_fp32(x, w, logits, T, H, E, err_flag, stream)
 
 @pytest.mark.parametrize("args,want", [
-    ((P, P, P, -1, 64, 16), L.MOE_ERR_INVALID_ARG),
-    ((P, P, P, 4, 0, 16), L.MOE_ERR_INVALID_ARG),
-    ((P, P, P, 4, 64, 0), L.MOE_ERR_INVALID_ARG),
-    ((P, P, P, 4, 60, 16), L.MOE_ERR_UNSUPPORTED),
-    ((P, P, P, 4, 64, 2048), L.MOE_ERR_UNSUPPORTED),
-    ((NULL, P, P, 4, 64, 16), L.MOE_ERR_INVALID_ARG),
-    ((P, NULL, P, 4, 64, 16), L.MOE_ERR_INVALID_ARG),
-    ((P, P, NULL, 4, 64, 16), L.MOE_ERR_INVALID_ARG),
-    ((P2, P, P, 4, 64, 16), L.MOE_ERR_MISALIGNED),
-    ((P, P2, P, 4, 64, 16), L.MOE_ERR_MISALIGNED),
-    ((P, P, P + 1, 4, 64, 16), L.MOE_ERR_MISALIGNED),
-    ((NULL, NULL, NULL, 0, 64, 16), L.MOE_OK),  # T == 0: nothing to do
+    ((P, P, P, -1, 64, 16, NULL), L.MOE_ERR_INVALID_ARG),
+    ((P, P, P, 4, 0, 16, NULL), L.MOE_ERR_INVALID_ARG),
+    ((P, P, P, 4, 64, 0, NULL), L.MOE_ERR_INVALID_ARG),
+    ((P, P, P, 4, 60, 16, NULL), L.MOE_ERR_UNSUPPORTED),
+    ((P, P, P, 4, 64, 2048, NULL), L.MOE_ERR_UNSUPPORTED),
+    ((NULL, P, P, 4, 64, 16, NULL), L.MOE_ERR_INVALID_ARG),
+    ((P, NULL, P, 4, 64, 16, NULL), L.MOE_ERR_INVALID_ARG),
+    ((P, P, NULL, 4, 64, 16, NULL), L.MOE_ERR_INVALID_ARG),
+    ((P2, P, P, 4, 64, 16, NULL), L.MOE_ERR_MISALIGNED),
+    ((P, P2, P, 4, 64, 16, NULL), L.MOE_ERR_MISALIGNED),
+    ((P, P, P + 1, 4, 64, 16, NULL), L.MOE_ERR_MISALIGNED),
+    ((P, P, P, 4, 64, 16, P + 2), L.MOE_ERR_MISALIGNED),
+    ((NULL, NULL, NULL, 0, 64, 16, NULL), L.MOE_OK),  # T == 0: nothing to do
 ])
 def test_router_argument_checks(lib, args, want):
     assert lib.moe_router_logits_fp32(*args, S) == want
@@ -188,6 +189,9 @@ def test_withhold_hook_argument_check(lib):
     # host-only: the request is stored for the next persistent-kernel launch
     assert lib.moe_debug_withhold_stream_stage(-2) == L.MOE_ERR_INVALID_ARG
     assert lib.moe_debug_withhold_stream_stage(-1) == L.MOE_OK
+    # the same for the next tensor-memory router launch
+    assert lib.moe_debug_withhold_router_stage(-2) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_debug_withhold_router_stage(-1) == L.MOE_OK
 
 
 def test_fail_next_launch_hook_argument_check(lib):

@@ -74,11 +74,61 @@ def test_router_logits(M, T, H, E):
     w = draw_bf16(rng, (E, H), 0.02)
     L, A = O.router_logits(x, w)
     out = Guarded((T, E), torch.float32)
-    M.moe_router_logits_fp32(dev(x), dev(w), logits_out=out.t)
-    out.check("logits")
+    flag = Guarded((1,), torch.int32, fill=0)
+    M.moe_router_logits_fp32(dev(x), dev(w), logits_out=out.t, err_flag=flag.t)
+    check_all(logits=out, err_flag=flag)
+    assert int(flag.t.item()) == 0
     g = out.t.cpu().numpy().astype(np.float64)
     err = np.abs(g - L)
     assert np.all(err <= 1e-5 * A + 1e-30), float(np.max(err / np.maximum(A, 1e-30)))
+
+
+@pytest.mark.parametrize("T,H", [(512, 2048), (8192, 512)])
+def test_router_wait_runs_out_and_the_next_launch_is_clean(M, T, H):
+    """The tensor-memory router's bounded waits: with one K block of the first
+    CTA withheld (test hook), that CTA's MMA warp gives up; its tile (the first
+    128 experts of the first token tile, whatever the split-K cluster) is
+    written as NaN and MOE_FLAG_TIMEOUT is set; every other logit is correct;
+    the next launch is correct and leaves the flag alone."""
+    import time
+
+    import moe_decode_layer_logits_gb300._lib as L
+    E = 256
+    rng = np.random.default_rng([104, T, H])
+    x = draw_bf16(rng, (T, H), 1.0)
+    w = draw_bf16(rng, (E, H), 0.02)
+    Lg, A = O.router_logits(x, w)
+    dx, dw = dev(x), dev(w)
+    out = Guarded((T, E), torch.float32)
+    flag = Guarded((1,), torch.int32, fill=0)
+    torch.cuda.synchronize()
+    M.moe_debug_withhold_router_stage(1)
+    t0 = time.perf_counter()
+    M.moe_router_logits_fp32(dx, dw, logits_out=out.t, err_flag=flag.t)
+    torch.cuda.synchronize()
+    _tol.EXTRA.append(f"withheld router K block (T={T}, H={H}): the launch gave up and completed after "
+                      f"{time.perf_counter() - t0:.3f} s")
+    check_all(logits=out, err_flag=flag)
+    assert int(flag.t.item()) & L.MOE_FLAG_TIMEOUT
+    g = out.t.cpu().numpy().astype(np.float64)
+    nan = np.isnan(g)
+    bnt = int(nan[:, 0].sum())  # the NaN rows: the first token tile
+    assert bnt in (64, 80, 96, 112, 128), bnt
+    want = np.zeros_like(nan)
+    want[:bnt, :128] = True
+    assert np.array_equal(nan, want)
+    ok = ~want
+    assert np.all(np.abs(g[ok] - Lg[ok]) <= 1e-5 * A[ok] + 1e-30)
+    # the next launch: correct, flag untouched
+    flag.t.zero_()
+    M.moe_router_logits_fp32(dx, dw, logits_out=out.t, err_flag=flag.t)
+    torch.cuda.synchronize()
+    check_all(logits=out, err_flag=flag)
+    assert int(flag.t.item()) == 0
+    g = out.t.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(g - Lg) <= 1e-5 * A + 1e-30)
+    with pytest.raises(L.MoeTailError):
+        M.moe_debug_withhold_router_stage(-2)
 
 
 def test_router_logits_misaligned_output(M):
