@@ -350,16 +350,6 @@ __device__ __forceinline__ bool stream_wait(uint64_t* bar, uint32_t parity, vola
   return false;
 }
 
-// Checked map entry of slot `lane` of token t, or -1 (flagged) if unusable.
-__device__ __forceinline__ int stream_map_entry(const TailParams& p, int64_t t, int lane) {
-  int m = p.map[t * p.k + lane];
-  if (m < 0 || static_cast<int64_t>(m) >= p.n_rows) {
-    if (p.err_flag) atomicOr(p.err_flag, MOE_FLAG_BAD_INDEX);
-    m = -1;
-  }
-  return m;
-}
-
 // A map entry if it names a row, else -1.
 __device__ __forceinline__ int in_rows(int m, int64_t n_rows) {
   return (m >= 0 && static_cast<int64_t>(m) < n_rows) ? m : -1;
@@ -539,24 +529,27 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
     // ------------------------------------------------------------ weights
     uint32_t keys[KEYS], keys_nxt[KEYS];
     float w_nxt = 0.f;
-    int ok_nxt = 0;
-    auto fetch = [&](int64_t t, uint32_t (&kk)[KEYS], float& w, int& ok) {
+    int m_nxt = -1;
+    // the next token's loads; its map entries are checked only where they are
+    // used, a token later, so that no load of the next token stalls the
+    // selection of this one
+    auto fetch = [&](int64_t t, uint32_t (&kk)[KEYS], float& w, int& m) {
       if (lane < k) {
-        ok = stream_map_entry(p, t, lane) >= 0;
+        m = p.map[t * k + lane];
         if (!ROUTE) w = p.topk_w[t * k + lane];
       }
       if (ROUTE) route_load_keys<KEYS>(p.logits + t * p.E, p.E, kk);
     };
-    if (ntok > 0) fetch(blockIdx.x, keys, w_nxt, ok_nxt);
+    if (ntok > 0) fetch(blockIdx.x, keys, w_nxt, m_nxt);
     for (int i = 0; i < ntok && !*abort_v; ++i) {
       const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(i) * G;
       float w = w_nxt;
-      const int ok = ok_nxt;
+      const int m_raw = m_nxt;
       if (ROUTE) {
 #pragma unroll
         for (int e = 0; e < KEYS; ++e) keys_nxt[e] = keys[e];
       }
-      if (i + 1 < ntok) fetch(t + G, keys, w_nxt, ok_nxt);  // next token's loads in flight
+      if (i + 1 < ntok) fetch(t + G, keys, w_nxt, m_nxt);  // next token's loads in flight
       if (ROUTE && lane == 0 && i + kLogitsAhead < ntok)
         prefetch_row_l2(p.logits + (t + static_cast<int64_t>(kLogitsAhead) * G) * p.E, p.E);
       if (ROUTE) {
@@ -567,6 +560,7 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
           if (p.w_out) p.w_out[t * k + lane] = w;
         }
       }
+      const int ok = lane < k && checked_entry(p, m_raw) >= 0;
       const int slot = i % kWRing, n = i / kWRing;
       if (n > 0 && !stream_wait(&wempty_bar[slot], (n - 1) & 1, abort_v, p.err_flag)) break;
       if (lane < k) w_ring[slot][lane] = ok ? w : 0.f;
