@@ -4,15 +4,23 @@
 // Details: the router folds the routed scaling factor into the weights).
 //
 // Lane l holds the logits of experts l, l + 32, ... as order-preserving
-// integer keys in registers, and the k experts are taken in k rounds.  With
-// at most 8 keys per lane, each lane first sorts its keys (descending, lower
-// expert first among equal keys, one 64-bit order on (key, inverted slot)),
-// and each round takes one warp max over the lanes' heads and a ballot of the
-// lanes holding it; a second reduction picks the lowest expert only when
-// several lanes tie; the winner pops its head.  Wider rows scan the lane's
-// keys each round, then two reductions pick the largest key and the lowest
-// expert holding it, and the winner clears its key.  Key 0 marks a taken or
-// padding slot: every finite logit has a key >= 1.
+// integer keys in registers.  With at most 8 keys per lane (E <= 256) and
+// k <= 16 the selection first bounds the k-th largest key from below: the
+// lanes form G >= k groups, and the smallest of the G group maxima, tau, is
+// exceeded or met by at least G >= k distinct keys, so every one of the top k
+// is >= tau, and so is every key that beats one of them.  The keys >= tau
+// (about 20 of 256 for k = 8 on Gaussian logits) are the candidates: ballots
+// give each its place in a shared-memory list, each candidate counts the
+// candidates that beat it (its rank), and the k best write themselves to
+// their rank's slot.  No chain of k dependent warp reductions is left.  For
+// larger k, or when more than kCandidateCap keys meet tau (heavy ties), the
+// selection takes sorted heads: each lane sorts its keys, and each of k rounds
+// takes one warp max over the lanes' heads, a ballot of the lanes holding it
+// (a second reduction picks the lowest expert only when several lanes tie),
+// and the winner pops its head.  Wider rows (E > 256) scan the lane's keys
+// each round, then two reductions pick the largest key and the lowest expert
+// holding it, and the winner clears its key.  Key 0 marks a taken or padding
+// slot: every finite logit has a key >= 1.
 #pragma once
 
 #include "common.cuh"
@@ -65,18 +73,93 @@ __device__ __forceinline__ void cx_desc(uint64_t& a, uint64_t& b) {
   a = hi;
 }
 
+// Candidate list of one routing warp: kCandidateCap entries, then the k
+// selected ones (shared memory, 16-byte aligned).
+constexpr int kCandidateCap = 64;
+constexpr int kRouteScratch = kCandidateCap + 32;
+
+// (key, expert) as one 64-bit value; a larger value is the better choice
+// (larger key, then lower expert).
+__device__ __forceinline__ uint64_t route_rank_value(uint32_t key, int expert) {
+  return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - static_cast<uint32_t>(expert));
+}
+
 // Select the top k (1 <= k <= min(E, 32)) of the logits loaded by
 // route_load_keys and weight them.  All 32 lanes call this; lane j < k
 // receives the j-th selected expert in `id` and its weight in `w`.  Consumes
-// `key`.
+// `key`.  `scratch` holds kRouteScratch entries of shared memory that only
+// this warp uses (for E <= 256, k <= 16), across calls; 16-byte aligned.
 template <int EPL>
-__device__ __forceinline__ void route_select(uint32_t (&key)[EPL], int k, float scale, int& id, float& w) {
+__device__ __forceinline__ void route_select(uint32_t (&key)[EPL], int k, float scale, int& id, float& w,
+                                             uint64_t* scratch) {
   const int lane = threadIdx.x & 31;
   route_bits_to_keys<EPL>(key);
   uint32_t my_key = 0u;
   int my_id = 0;
   int rounds = k;
   if constexpr (EPL <= 8) {
+    if (k <= 16) {
+      // tau: the smallest of G group maxima, G = 8 or 16 >= k groups of 4 or
+      // 2 lanes (larger k leaves too many candidates: sorted heads below)
+      uint32_t gm = key[0];
+#pragma unroll
+      for (int s = 1; s < EPL; ++s) gm = key[s] > gm ? key[s] : gm;
+      for (int d = 1; d < 32 && (32 / (2 * d)) >= k; d <<= 1) {
+        const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, gm, d);
+        gm = o > gm ? o : gm;
+      }
+      const uint32_t tau = __reduce_min_sync(0xFFFFFFFFu, gm);
+      // the candidates' places in the list: slot-major, lanes in order
+      // (ascending expert); places past the cap are not written, and a list
+      // that would overflow is not used
+      uint32_t below;
+      asm("mov.u32 %0, %%lanemask_lt;" : "=r"(below));
+      uint32_t bal[EPL];
+#pragma unroll
+      for (int s = 0; s < EPL; ++s) bal[s] = __ballot_sync(0xFFFFFFFFu, key[s] >= tau);
+      __syncwarp();  // an earlier call's accesses to the list are complete
+      int n = 0;
+#pragma unroll
+      for (int s = 0; s < EPL; ++s) {
+        const int at = n + __popc(bal[s] & below);
+        if (key[s] >= tau && at < kCandidateCap) scratch[at] = route_rank_value(key[s], lane + 32 * s);
+        n += __popc(bal[s]);
+      }
+      if (n <= kCandidateCap) {
+        // rank = how many candidates beat this one; the values are distinct
+        // (one per expert), so the ranks are 0 .. n-1, each once.  The list
+        // is padded with 0 (below every candidate) to whole blocks of 8, and
+        // each lane ranks candidates lane and lane + 32 in one pass.
+        const int nb = (n + 7) >> 3;
+        __syncwarp();
+        if (n + lane < 8 * nb) scratch[n + lane] = 0ull;
+        __syncwarp();
+        const ulonglong2* list = reinterpret_cast<const ulonglong2*>(scratch);
+        const uint64_t v0 = lane < n ? scratch[lane] : ~0ull;
+        const uint64_t v1 = lane + 32 < n ? scratch[lane + 32] : ~0ull;
+        int r0 = 0, r1 = 0;
+        for (int b = 0; b < nb; ++b) {
+          ulonglong2 c[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) c[i] = list[4 * b + i];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            r0 += (c[i].x > v0 ? 1 : 0) + (c[i].y > v0 ? 1 : 0);
+            r1 += (c[i].x > v1 ? 1 : 0) + (c[i].y > v1 ? 1 : 0);
+          }
+        }
+        uint64_t* chosen = scratch + kCandidateCap;
+        if (lane < n && r0 < k) chosen[r0] = v0;
+        if (lane + 32 < n && r1 < k) chosen[r1] = v1;
+        __syncwarp();
+        if (lane < k) {
+          const uint64_t v = chosen[lane];
+          my_key = static_cast<uint32_t>(v >> 32);
+          my_id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(v));
+        }
+        rounds = 0;
+      }
+    }
     if (rounds > 0) {
       // Sorted heads: each lane sorts its candidates once (descending key,
       // ascending slot among equal keys), then every round needs one warp
@@ -149,10 +232,10 @@ __device__ __forceinline__ void route_select(uint32_t (&key)[EPL], int k, float 
 // Both phases for one token row.
 template <int EPL>
 __device__ __forceinline__ void warp_route(const float* __restrict__ row, int E, int k, float scale,
-                                           int& id, float& w) {
+                                           int& id, float& w, uint64_t* scratch) {
   uint32_t key[EPL];
   route_load_keys<EPL>(row, E, key);
-  route_select<EPL>(key, k, scale, id, w);
+  route_select<EPL>(key, k, scale, id, w, scratch);
 }
 
 }  // namespace moe

@@ -56,6 +56,7 @@ tail_kernel(const TailParams p) {
   __shared__ float red[33];
   __shared__ float cluster_slots[8 * (kMaxThreads / 32)];  // [cluster rank][warp]
   __shared__ uint64_t ss_bar;  // split rows: completes when every CTA's warp sums have landed
+  __shared__ __align__(16) uint64_t route_scr[EPL > 0 ? kRouteScratch : 1];  // the routing warp's candidate list
 
   const int t = blockIdx.y;
   const int tid = threadIdx.x;
@@ -178,7 +179,7 @@ tail_kernel(const TailParams p) {
       if (tid < 32) {
         int id;
         float w;
-        route_select<KEYS>(keys, k, p.scale, id, w);
+        route_select<KEYS>(keys, k, p.scale, id, w, route_scr);
         if (tid < k) {
           w_s[tid] = map_s[tid] < 0 ? 0.f : w;  // an unusable slot adds exactly nothing
           if (rank == 0) {
@@ -406,6 +407,7 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
   __shared__ uint64_t wempty_bar[kWRing];
   __shared__ float w_ring[kWRing][MOE_MAX_K];
   __shared__ float red[2][kStreamConsumerWarps];
+  __shared__ __align__(16) uint64_t route_scr[EPL > 0 ? kRouteScratch : 1];  // the weights warp's candidate list
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -554,7 +556,7 @@ tail_stream_kernel(const TailParams p, const int T, const StreamShape sh) {
         prefetch_row_l2(p.logits + (t + static_cast<int64_t>(kLogitsAhead) * G) * p.E, p.E);
       if (ROUTE) {
         int id;
-        route_select<KEYS>(keys_nxt, k, p.scale, id, w);  // runs ahead of the consumers
+        route_select<KEYS>(keys_nxt, k, p.scale, id, w, route_scr);  // runs ahead of the consumers
         if (lane < k) {
           if (p.ids_out) p.ids_out[t * k + lane] = id;
           if (p.w_out) p.w_out[t * k + lane] = w;
@@ -747,7 +749,9 @@ static cudaError_t launch_tail_v(const TailParams& p, int T, const TailLaunch& L
   }
   cfg.attrs = attr;
   cfg.numAttrs = nattr;
-  return cudaLaunchKernelEx(&cfg, tail_kernel<VPT, 8, EPL>, p);
+  // 4 vectors a thread gather 4 slots a batch (16 loads in flight a thread):
+  // 8 would not fit the registers beside the routing warp's selection
+  return cudaLaunchKernelEx(&cfg, tail_kernel<VPT, (VPT >= 4 ? 4 : 8), EPL>, p);
 }
 
 template <int EPL>

@@ -11,6 +11,7 @@ template <int EPL>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 topk_route_kernel(const float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ wts,
                   int T, int E, int k, float scale) {
+  __shared__ __align__(16) uint64_t route_scr[kRouteWarps][kRouteScratch];  // each warp's candidate list
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRouteWarps + warp;
   allow_dependent_launch();
@@ -18,7 +19,7 @@ topk_route_kernel(const float* __restrict__ logits, int32_t* __restrict__ ids, f
   if (t >= T) return;  // whole warp leaves together; the kernel has no block barrier
   int id;
   float w;
-  warp_route<EPL>(logits + static_cast<int64_t>(t) * E, E, k, scale, id, w);
+  warp_route<EPL>(logits + static_cast<int64_t>(t) * E, E, k, scale, id, w, route_scr[warp]);
   if (lane < k) {
     ids[static_cast<int64_t>(t) * k + lane] = id;
     wts[static_cast<int64_t>(t) * k + lane] = w;

@@ -279,6 +279,8 @@ FIN = [  # name, T, H, E, k, extra kwargs
     ("h8", 3, 8, 16, 2, dict(seed=12)),
     ("h16384", 3, 16384, 16, 8, dict(seed=13)),
     ("h65536", 2, 65536, 16, 4, dict(seed=14)),
+    # 4 vectors a thread on one CTA a row: the slots are gathered 4 at a time
+    ("h8192-t160", 160, 8192, 64, 8, dict(seed=31)),
     ("t300", 300, 2048, 16, 8, dict(seed=15)),
     # batches of >= 2 tokens per SM take the persistent bulk-copy kernel
     ("stream-ragged-h", 400, 2056, 72, 5, dict(seed=16)),
@@ -556,6 +558,7 @@ FUSED = [  # name, T, H, E, k, kw
     ("ragged", 37, 2056, 72, 3, dict(seed=8)),
     ("no-shared", 5, 1024, 1024, 32, dict(seed=9, shared=False)),
     ("e1", 3, 64, 1, 1, dict(seed=10)),
+    ("h8192-t160", 160, 8192, 256, 8, dict(seed=15)),
     ("stream-e1024", 320, 1024, 1024, 32, dict(seed=11)),
     ("stream-ragged", 400, 2056, 72, 3, dict(seed=12, shared=False)),
     # the real checkpoint's 168 experts, and an expert-grouped row layout
