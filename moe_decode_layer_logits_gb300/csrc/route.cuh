@@ -161,7 +161,7 @@ __device__ __forceinline__ void route_select(uint32_t (&key)[EPL], int k, float 
       }
     }
     if (rounds > 0) {
-      // Sorted heads: each lane sorts its candidates once (descending key,
+      // Sorted heads: each lane sorts its keys once (descending key,
       // ascending slot among equal keys), then every round needs one warp
       // max over the lanes' heads and a ballot; only when several lanes tie
       // on that key does a second reduction pick the lowest expert.

@@ -96,8 +96,14 @@ tail_kernel(const TailParams p) {
   }
   grid_dependency_wait();
 
-  // the slot table's loads go first (every row gather waits for them),
-  // pinned here and consumed at the slot table below
+  // router-less variant: warp 0 requests the token's logits first (the
+  // selection waits for them, and it overlaps the expert-row gathers)
+  constexpr int KEYS = EPL > 0 ? EPL : 1;
+  uint32_t keys[KEYS];
+  if (ROUTE && tid < 32) route_load_keys<KEYS>(p.logits + static_cast<int64_t>(t) * p.E, p.E, keys);
+
+  // then the slot table's loads (every row gather waits for them), pinned
+  // here and consumed at the slot table below
   int map_raw = -1;
   uint32_t w_raw = 0u;
   if (tid < k) {
@@ -105,12 +111,6 @@ tail_kernel(const TailParams p) {
     asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(map_raw) : "l"(mp));
     if (!ROUTE) asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(w_raw) : "l"(p.topk_w + static_cast<int64_t>(t) * k + tid));
   }
-
-  // router-less variant: warp 0 requests the token's logits next, so the
-  // selection below overlaps the expert-row gathers
-  constexpr int KEYS = EPL > 0 ? EPL : 1;
-  uint32_t keys[KEYS];
-  if (ROUTE && tid < 32) route_load_keys<KEYS>(p.logits + static_cast<int64_t>(t) * p.E, p.E, keys);
 
   int vidx[VPT];
   bool vok[VPT];
