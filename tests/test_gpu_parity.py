@@ -180,6 +180,8 @@ def test_router_small_integers_exact(M):
 ROUTE = [  # (T, E, k, scale)
     (4, 64, 4, 1.0), (1, 256, 8, 2.5), (64, 256, 8, 2.5), (8192, 256, 8, 2.5), (37, 72, 3, 1.0),
     (5, 1024, 32, 0.5), (7, 33, 32, 2.5), (3, 1, 1, 2.5), (11, 168, 8, 2.5), (9, 40, 32, 1.0),
+    # k = 9 .. 16 bound the k-th largest logit with 16 groups of 2 lanes
+    (33, 256, 16, 1.5), (17, 100, 12, 1.0), (5, 256, 9, 2.5),
 ]
 
 
@@ -203,7 +205,7 @@ def test_topk_route(M, T, E, k, scale):
     _check_route(M, lg, k, scale)
 
 
-@pytest.mark.parametrize("E,k", [(64, 4), (256, 8), (9, 5)])
+@pytest.mark.parametrize("E,k", [(64, 4), (256, 8), (9, 5), (256, 16), (200, 3)])
 def test_topk_route_ties(M, E, k):
     # integer logits in [-2, 2]: many exact ties, resolved to the lower index
     rng = np.random.default_rng([201, E, k])
@@ -559,6 +561,8 @@ FUSED = [  # name, T, H, E, k, kw
     ("no-shared", 5, 1024, 1024, 32, dict(seed=9, shared=False)),
     ("e1", 3, 64, 1, 1, dict(seed=10)),
     ("h8192-t160", 160, 8192, 256, 8, dict(seed=15)),
+    ("k16", 20, 2048, 256, 16, dict(seed=16)),
+    ("stream-k12", 320, 1024, 256, 12, dict(seed=17)),
     ("stream-e1024", 320, 1024, 1024, 32, dict(seed=11)),
     ("stream-ragged", 400, 2056, 72, 3, dict(seed=12, shared=False)),
     # the real checkpoint's 168 experts, and an expert-grouped row layout
